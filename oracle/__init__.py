@@ -1,0 +1,202 @@
+"""fp64 CPU oracle of the linear GRPO loss -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The library (``rl_fine_tuning_gb300``)
+neither imports nor links it, and shares no code with it.
+
+The arithmetic lives in ``grpo_oracle.c`` (plain loops, fp64, ascending-index
+sums).  This module only compiles it and marshals numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libgrpo_oracle.so")
+
+TYPE_CODE = {"f64": 0, "bf16": 1, "fp16": 2}
+ROW_FIELDS = ("lse_pol", "lse_ref", "zt_pol", "zt_ref", "q", "p", "kl", "ell", "g")
+
+
+def build(force: bool = False) -> str:
+    src = os.path.join(_HERE, "grpo_oracle.c")
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
+        os.makedirs(_BUILD, exist_ok=True)
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", src, "-o", tmp, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+_lib = None
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        p, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_set_threads.argtypes = [i32]
+        lib.oracle_max_threads.restype = i32
+        lib.oracle_bf16_to_f64.restype = f64
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f64.restype = f64
+        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_group_advantages.argtypes = [p, i32, i32, ctypes.c_float, i32, p]
+        lib.oracle_build_mask.argtypes = [p, i32, i32, p]
+        lib.oracle_valid_rows.restype = i64
+        lib.oracle_valid_rows.argtypes = [p, i64, p]
+        lib.oracle_logsumexp.restype = f64
+        lib.oracle_logsumexp.argtypes = [p, i32]
+        lib.oracle_row_terms.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, p, i64, p]
+        lib.oracle_loss.restype = f64
+        lib.oracle_loss.argtypes = [p, p, p, i32, p, p, p, i64, i32, i32, i32, f64, p]
+        lib.oracle_surrogate.restype = f64
+        lib.oracle_surrogate.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, p, i64, p, f64]
+        lib.oracle_grad.argtypes = [p, p, i32, p, i32, i32, p, i64, p, p, f64, p, p, i64, p]
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle wants C-contiguous arrays"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def set_threads(n: int):
+    _L().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_L().oracle_max_threads())
+
+
+def _mat(a, dtype):
+    """H / W argument: uint16 bit patterns for bf16/fp16, float64 for f64."""
+    if dtype == "f64":
+        return np.ascontiguousarray(a, np.float64)
+    return np.ascontiguousarray(a, np.uint16)
+
+
+def group_advantages(rewards, n_groups, G, eps=1e-4, std_unbiased=True):
+    r = np.ascontiguousarray(rewards, np.float32)
+    out = np.empty(n_groups * G, np.float32)
+    _L().oracle_group_advantages(_p(r), n_groups, G, eps, int(bool(std_unbiased)), _p(out))
+    return out
+
+
+def build_mask(lengths, L):
+    lens = np.ascontiguousarray(lengths, np.int32)
+    out = np.empty(lens.size * L, np.uint8)
+    _L().oracle_build_mask(_p(lens), lens.size, L, _p(out))
+    return out
+
+
+def valid_rows(mask):
+    m = np.ascontiguousarray(mask, np.uint8)
+    out = np.empty(max(m.size, 1), np.int32)
+    n = _L().oracle_valid_rows(_p(m), m.size, _p(out))
+    return out[:n].copy()
+
+
+def logsumexp(z):
+    z = np.ascontiguousarray(z, np.float64)
+    return float(_L().oracle_logsumexp(_p(z), z.size))
+
+
+def row_terms(h_pol, h_ref, W, dtype, tokens, adv, L, rows, beta=0.04, W_ref=None):
+    """Per-row forward terms for the listed rows -> dict of float64 arrays."""
+    h_pol, h_ref, W = _mat(h_pol, dtype), _mat(h_ref, dtype), _mat(W, dtype)
+    Wr = None if W_ref is None else _mat(W_ref, dtype)
+    V, d = W.shape
+    tok = np.ascontiguousarray(tokens, np.int32)
+    adv = np.ascontiguousarray(adv, np.float32)
+    rows = np.ascontiguousarray(rows, np.int32)
+    out = np.empty((rows.size, 9), np.float64)
+    _L().oracle_row_terms(_p(h_pol), _p(h_ref), _p(W), _p(Wr), TYPE_CODE[dtype], _p(tok), _p(adv),
+                          L, d, V, beta, _p(rows), rows.size, _p(out))
+    return {k: out[:, i].copy() for i, k in enumerate(ROW_FIELDS)}
+
+
+def loss(h_pol, h_ref, W, dtype, tokens, mask, adv, L, beta=0.04):
+    """Masked token-mean loss and N_v."""
+    h_pol, h_ref, W = _mat(h_pol, dtype), _mat(h_ref, dtype), _mat(W, dtype)
+    V, d = W.shape
+    tok = np.ascontiguousarray(tokens, np.int32)
+    mask = np.ascontiguousarray(mask, np.uint8)
+    adv = np.ascontiguousarray(adv, np.float32)
+    nv = ctypes.c_int64(0)
+    val = _L().oracle_loss(_p(h_pol), _p(h_ref), _p(W), TYPE_CODE[dtype], _p(tok), _p(mask), _p(adv),
+                           mask.size, L, d, V, beta, ctypes.byref(nv))
+    return float(val), int(nv.value)
+
+
+def surrogate(h_pol, h_ref, W, dtype, tokens, adv, L, rows, c, w, beta=0.04, W_ref=None):
+    """w * sum_i [-A exp(q_i - c_i) + beta KL_i]; c=None re-evaluates c = q (no detach).
+
+    W_ref: weight of the frozen reference (None: W itself)."""
+    h_pol, h_ref, W = _mat(h_pol, dtype), _mat(h_ref, dtype), _mat(W, dtype)
+    Wr = None if W_ref is None else _mat(W_ref, dtype)
+    V, d = W.shape
+    tok = np.ascontiguousarray(tokens, np.int32)
+    adv = np.ascontiguousarray(adv, np.float32)
+    rows = np.ascontiguousarray(rows, np.int32)
+    cc = None if c is None else np.ascontiguousarray(c, np.float64)
+    return float(_L().oracle_surrogate(_p(h_pol), _p(h_ref), _p(W), _p(Wr), TYPE_CODE[dtype], _p(tok),
+                                       _p(adv), L, d, V, beta, _p(rows), rows.size, _p(cc), w))
+
+
+def grad(h_pol, W, dtype, tokens, rows, lse, g, w, want_dH=True, vrows=None, want_dW=True):
+    """dH for the listed rows ([n_rows, d]) and dW for vocabulary rows vrows (all if None)."""
+    h_pol, W = _mat(h_pol, dtype), _mat(W, dtype)
+    V, d = W.shape
+    tok = np.ascontiguousarray(tokens, np.int32)
+    rows = np.ascontiguousarray(rows, np.int32)
+    lse = np.ascontiguousarray(lse, np.float64)
+    g = np.ascontiguousarray(g, np.float64)
+    dH = np.empty((rows.size, d), np.float64) if want_dH else None
+    vr = None if vrows is None else np.ascontiguousarray(vrows, np.int32)
+    n_v = V if vr is None else vr.size
+    dW = np.empty((n_v, d), np.float64) if want_dW else None
+    _L().oracle_grad(_p(h_pol), _p(W), TYPE_CODE[dtype], _p(tok), d, V, _p(rows), rows.size,
+                     _p(lse), _p(g), w, _p(dH), _p(vr), 0 if vr is None else vr.size, _p(dW))
+    return dH, dW
+
+
+def expected(wl, eval_rows=None, vrows=None, mask=None, want_dH=True, want_dW=True,
+             std_unbiased=True):
+    """Everything the library computes for a synthetic workload, in fp64.
+
+    eval_rows: the valid rows whose per-row terms (and dH) are computed; None
+    means every valid row, in which case the loss is the full masked mean.
+    mask: overrides the mask built from the workload's lengths.
+    """
+    cfg = wl.cfg
+    adv = group_advantages(wl.rewards, cfg.n_groups, cfg.G, cfg.eps, std_unbiased)
+    if mask is None:
+        mask = build_mask(wl.lengths, cfg.L)
+    rows_all = valid_rows(mask)
+    n_valid = rows_all.size
+    w = 1.0 / max(n_valid, 1)
+    full = eval_rows is None
+    rows = rows_all if full else np.ascontiguousarray(eval_rows, np.int32)
+    terms = row_terms(wl.h_pol, wl.h_ref, wl.W, cfg.dtype, wl.tokens, adv, cfg.L, rows, cfg.beta)
+    out = dict(adv=adv, mask=mask, rows=rows_all, n_valid=n_valid, w=w, eval_rows=rows, terms=terms)
+    if full:
+        # exactly rounded sum of the per-row terms, then the token mean
+        out["loss"] = math.fsum(terms["ell"].tolist()) / n_valid if n_valid else 0.0
+    if want_dH or want_dW:
+        dH, dW = grad(wl.h_pol, wl.W, cfg.dtype, wl.tokens, rows, terms["lse_pol"], terms["g"], w,
+                      want_dH=want_dH, vrows=vrows, want_dW=want_dW and full)
+        out["dH"] = dH
+        out["dW"] = dW
+    return out

@@ -1,0 +1,299 @@
+/*
+ * Plain fp64 CPU oracle of the memory-efficient ("linear") GRPO loss.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the CPU baseline
+ * leg of the benchmark call this code to obtain expected values; the library
+ * itself never links, loads or calls it, and the two share no code.
+ *
+ * What is computed, and where the pages fix it:
+ *   - Group-relative advantages: responses of one prompt form a group; each
+ *     reward is compared with the group mean and the better responses are
+ *     reinforced ("Train your own R1 reasoning model with Unsloth", section 3,
+ *     steps 3-5).  The spread normaliser (sample std + eps) is the reading the
+ *     workload definitions take; the pages print no formula.
+ *   - Token log-probabilities of the sampled tokens under the trained policy
+ *     (q) and the frozen reference (p), computed from the lm_head logits with
+ *     the logsumexp trick ("Long-context GRPO", section 4, last paragraph).
+ *     The linear algorithm never stores the logits; it reaches exactly the
+ *     same numbers as materialising them ("Long-context GRPO", section 2),
+ *     so the oracle is that plain definition.
+ *   - Per-token objective with the policy-gradient factor exp(q - sg(q)) * A,
+ *     whose value is A and whose gradient w.r.t. q is A ("Long-context GRPO",
+ *     section 4, the detach fragment), and the reverse-KL penalty with
+ *     beta = 0.04 in its unbiased form exp(p-q) - (p-q) - 1 that needs no
+ *     extra Q factor (same section).  KL is evaluated as expm1(x) - x.
+ *   - Mean over completion tokens (mask), gradient to the hidden states and
+ *     to the lm_head weight.
+ *
+ * Everything is fp64 on inputs widened exactly from their storage type
+ * (bf16 / fp16 / double).  Sums run in ascending index order.  OpenMP only
+ * splits independent rows (or independent vocabulary rows for dW) across
+ * threads, so results do not depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_F64 = 0, OR_BF16 = 1, OR_F16 = 2 };
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ---- exact widening of the storage types -------------------------------- */
+
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+double oracle_f16_to_f64(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 10) & 31;
+    int m = b & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);                 /* subnormal / zero */
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+static inline double ld(const void* p, int type, size_t i) {
+    if (type == OR_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[i]);
+    if (type == OR_F16) return oracle_f16_to_f64(((const uint16_t*)p)[i]);
+    return ((const double*)p)[i];
+}
+
+/* ---- advantages ---------------------------------------------------------- */
+
+/* rewards [n_groups*G] -> adv [n_groups*G]; fp64 with left-to-right sums,
+ * rounded once to fp32.  sigma uses divisor G-1 (std_unbiased) or G; a group
+ * whose divisor is 0 has sigma = 0. */
+void oracle_group_advantages(const float* rewards, int n_groups, int G, float eps,
+                             int std_unbiased, float* adv) {
+    for (int gi = 0; gi < n_groups; ++gi) {
+        const float* r = rewards + (size_t)gi * G;
+        double sum = 0.0;
+        for (int i = 0; i < G; ++i) sum = sum + (double)r[i];
+        double mu = sum / (double)G;
+        double ss = 0.0;
+        for (int i = 0; i < G; ++i) {
+            double dv = (double)r[i] - mu;
+            ss = ss + dv * dv;
+        }
+        int div = std_unbiased ? G - 1 : G;
+        double sigma = div > 0 ? sqrt(ss / (double)div) : 0.0;
+        double den = sigma + (double)eps;
+        for (int i = 0; i < G; ++i) adv[(size_t)gi * G + i] = (float)(((double)r[i] - mu) / den);
+    }
+}
+
+/* ---- mask and valid-row index -------------------------------------------- */
+
+/* completion i occupies positions j < len_i of its L-row block */
+void oracle_build_mask(const int32_t* lengths, int n_seq, int L, uint8_t* mask) {
+    for (int i = 0; i < n_seq; ++i)
+        for (int j = 0; j < L; ++j) mask[(size_t)i * L + j] = (uint8_t)(j < lengths[i]);
+}
+
+int64_t oracle_valid_rows(const uint8_t* mask, int64_t N, int32_t* rows) {
+    int64_t n = 0;
+    for (int64_t t = 0; t < N; ++t)
+        if (mask[t]) {
+            if (rows) rows[n] = (int32_t)t;
+            ++n;
+        }
+    return n;
+}
+
+/* ---- logits of one row and their logsumexp ------------------------------ */
+
+/* widen row r of a [*, d] matrix into out[d] */
+static void load_row(const void* M, int type, int64_t r, int d, double* out) {
+    for (int k = 0; k < d; ++k) out[k] = ld(M, type, (size_t)r * d + k);
+}
+
+/* dot(h, W[v,:]) with h already widened; sum in ascending k */
+static inline double dot_w(const double* h, const void* W, int type, int v, int d) {
+    double acc = 0.0;
+    if (type == OR_BF16) {
+        const uint16_t* w = (const uint16_t*)W + (size_t)v * d;
+        for (int k = 0; k < d; ++k) acc = acc + h[k] * oracle_bf16_to_f64(w[k]);
+    } else if (type == OR_F16) {
+        const uint16_t* w = (const uint16_t*)W + (size_t)v * d;
+        for (int k = 0; k < d; ++k) acc = acc + h[k] * oracle_f16_to_f64(w[k]);
+    } else {
+        const double* w = (const double*)W + (size_t)v * d;
+        for (int k = 0; k < d; ++k) acc = acc + h[k] * w[k];
+    }
+    return acc;
+}
+
+/* z[v] = sum_k h[t,k] * W[v,k] for all v (hrow: scratch of d doubles) */
+static void row_logits(const void* H, const void* W, int type, int64_t t, int d, int V, double* z,
+                       double* hrow) {
+    load_row(H, type, t, d, hrow);
+    for (int v = 0; v < V; ++v) z[v] = dot_w(hrow, W, type, v, d);
+}
+
+/* log sum_v exp(z_v), computed as m + log sum exp(z - m) */
+double oracle_logsumexp(const double* z, int V) {
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) m = z[v] > m ? z[v] : m;
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) s = s + exp(z[v] - m);
+    return m + log(s);
+}
+
+/* ---- per-row forward terms ----------------------------------------------- */
+
+/* out[i*9 + .] for row t = rows[i]:
+ *   0 lse_pol  1 lse_ref  2 z_pol[tok]  3 z_ref[tok]  4 q  5 p  6 kl  7 ell  8 g
+ * adv is per sequence; row t belongs to sequence t / L.
+ * The reference logits use W_ref (NULL: the same W).  The frozen reference
+ * is a constant of the objective: no gradient is taken through it. */
+void oracle_row_terms(const void* h_pol, const void* h_ref, const void* W, const void* W_ref,
+                      int type, const int32_t* tokens, const float* adv, int L, int d, int V,
+                      double beta, const int32_t* rows, int64_t n_rows, double* out) {
+    if (!W_ref) W_ref = W;
+#pragma omp parallel
+    {
+        double* z = (double*)malloc(sizeof(double) * (size_t)V);
+        double* hrow = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < n_rows; ++i) {
+            int64_t t = rows[i];
+            int tok = tokens[t];
+            double A = (double)adv[t / L];
+            row_logits(h_pol, W, type, t, d, V, z, hrow);
+            double lse_pol = oracle_logsumexp(z, V);
+            double zt_pol = z[tok];
+            row_logits(h_ref, W_ref, type, t, d, V, z, hrow);
+            double lse_ref = oracle_logsumexp(z, V);
+            double zt_ref = z[tok];
+            double q = zt_pol - lse_pol;
+            double p = zt_ref - lse_ref;
+            double x = p - q;
+            double kl = expm1(x) - x;                 /* exp(x) - x - 1 */
+            double ell = -A + beta * kl;              /* value of -[exp(q-sg q) A - beta KL] */
+            double g = -A - beta * expm1(x);          /* d ell / d q = -A + beta (1 - e^x) */
+            double* o = out + (size_t)i * 9;
+            o[0] = lse_pol; o[1] = lse_ref; o[2] = zt_pol; o[3] = zt_ref;
+            o[4] = q; o[5] = p; o[6] = kl; o[7] = ell; o[8] = g;
+        }
+        free(hrow);
+        free(z);
+    }
+}
+
+/* loss = sum over masked rows of ell / max(N_v, 1); also returns N_v */
+double oracle_loss(const void* h_pol, const void* h_ref, const void* W, int type,
+                   const int32_t* tokens, const uint8_t* mask, const float* adv,
+                   int64_t N, int L, int d, int V, double beta, int64_t* n_valid_out) {
+    int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
+    int64_t nv = oracle_valid_rows(mask, N, rows);
+    double* terms = (double*)malloc(sizeof(double) * 9 * (size_t)(nv > 0 ? nv : 1));
+    oracle_row_terms(h_pol, h_ref, W, NULL, type, tokens, adv, L, d, V, beta, rows, nv, terms);
+    double s = 0.0;
+    for (int64_t i = 0; i < nv; ++i) s = s + terms[(size_t)i * 9 + 7];
+    free(terms);
+    free(rows);
+    if (n_valid_out) *n_valid_out = nv;
+    return nv > 0 ? s / (double)nv : 0.0;
+}
+
+/* Surrogate objective whose gradient is the GRPO gradient:
+ *   J = w * sum_i [ -A exp(q_i - c_i) + beta (exp(p_i-q_i) - (p_i-q_i) - 1) ]
+ * With c held at q's value this is the detached objective; passing
+ * c == NULL re-evaluates c = q inside, i.e. the variant without the detach. */
+double oracle_surrogate(const void* h_pol, const void* h_ref, const void* W, const void* W_ref,
+                        int type, const int32_t* tokens, const float* adv, int L, int d, int V,
+                        double beta, const int32_t* rows, int64_t n_rows, const double* c, double w) {
+    double* terms = (double*)malloc(sizeof(double) * 9 * (size_t)(n_rows > 0 ? n_rows : 1));
+    oracle_row_terms(h_pol, h_ref, W, W_ref, type, tokens, adv, L, d, V, beta, rows, n_rows, terms);
+    double s = 0.0;
+    for (int64_t i = 0; i < n_rows; ++i) {
+        const double* o = terms + (size_t)i * 9;
+        double A = (double)adv[rows[i] / L];
+        double ci = c ? c[i] : o[4];
+        s = s + (-A * exp(o[4] - ci) + beta * o[6]);
+    }
+    free(terms);
+    return w * s;
+}
+
+/* ---- backward ------------------------------------------------------------ */
+
+/* dS[t,v] = w * g_t * (1[v == tok_t] - exp(z_tv - lse_t)) for the policy logits.
+ *   dH[i,:] = sum_v dS[rows[i], v] * W[v,:]                 (if dH != NULL)
+ *   dW[j,:] = sum_i dS[rows[i], vrows[j]] * h_pol[rows[i],:] (if dW != NULL;
+ *             vrows == NULL means all V vocabulary rows in order)
+ * lse and g are per listed row (from oracle_row_terms). */
+void oracle_grad(const void* h_pol, const void* W, int type, const int32_t* tokens,
+                 int d, int V, const int32_t* rows, int64_t n_rows,
+                 const double* lse, const double* g, double w,
+                 double* dH, const int32_t* vrows, int64_t n_vrows, double* dW) {
+    if (dH) {
+#pragma omp parallel
+        {
+            double* z = (double*)malloc(sizeof(double) * (size_t)V);
+            double* hrow = (double*)malloc(sizeof(double) * (size_t)d);
+            double* wrow = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t i = 0; i < n_rows; ++i) {
+                int64_t t = rows[i];
+                int tok = tokens[t];
+                double* out = dH + (size_t)i * d;
+                row_logits(h_pol, W, type, t, d, V, z, hrow);
+                for (int k = 0; k < d; ++k) out[k] = 0.0;
+                for (int v = 0; v < V; ++v) {
+                    double dS = w * g[i] * ((v == tok ? 1.0 : 0.0) - exp(z[v] - lse[i]));
+                    load_row(W, type, v, d, wrow);
+                    for (int k = 0; k < d; ++k) out[k] = out[k] + dS * wrow[k];
+                }
+            }
+            free(wrow);
+            free(hrow);
+            free(z);
+        }
+    }
+    if (dW) {
+        int64_t nv = vrows ? n_vrows : V;
+#pragma omp parallel
+        {
+            double* hrow = (double*)malloc(sizeof(double) * (size_t)d);
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t j = 0; j < nv; ++j) {
+                int v = vrows ? vrows[j] : (int)j;
+                double* out = dW + (size_t)j * d;
+                for (int k = 0; k < d; ++k) out[k] = 0.0;
+                for (int64_t i = 0; i < n_rows; ++i) {
+                    int64_t t = rows[i];
+                    load_row(h_pol, type, t, d, hrow);
+                    double z = dot_w(hrow, W, type, v, d);
+                    double dS = w * g[i] * ((v == tokens[t] ? 1.0 : 0.0) - exp(z - lse[i]));
+                    for (int k = 0; k < d; ++k) out[k] = out[k] + dS * hrow[k];
+                }
+            }
+            free(hrow);
+        }
+    }
+}
