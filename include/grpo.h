@@ -1,0 +1,160 @@
+/*
+ * libgrpo -- fused memory-efficient ("linear") GRPO loss for one NVIDIA GB300
+ * (sm_103a).  C ABI: plain pointers and sizes, no framework types.
+ *
+ * The operation ("Long-context GRPO", sections 2-4; "Train your own R1
+ * reasoning model with Unsloth", section 3):
+ *
+ *   For every completion token t (row t of the hidden-state matrices),
+ *     z_pol = h_pol[t] . W^T      z_ref = h_ref[t] . W^T      (V logits each)
+ *     q_t = z_pol[tok_t] - logsumexp(z_pol)    policy log-prob of the sampled token
+ *     p_t = z_ref[tok_t] - logsumexp(z_ref)    frozen-reference log-prob
+ *     ell_t = -[ exp(q_t - sg(q_t)) * A_i - beta * (exp(p_t-q_t) - (p_t-q_t) - 1) ]
+ *   with A_i the group-relative advantage of the completion (sequence) i that
+ *   row t belongs to, and the loss is the mean of ell_t over masked rows.
+ *   The backward gives dH = d loss / d h_pol and dW = d loss / d W through the
+ *   policy logits (the reference is a frozen constant).
+ *
+ *   The (rows x V) logits are never stored: extra device memory is
+ *   O(chunk_rows * V + rows), never O(rows * V).
+ *
+ * Conventions shared by every entry point
+ *   - All data pointers are caller-owned DEVICE memory; the library never
+ *     allocates or frees device memory and keeps no pointer after a call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; 0 = legacy default
+ *     stream).  The return value reports argument validation and launch
+ *     errors only; errors found while the kernels run are written to the
+ *     caller's device word `status` (same codes), which the call resets to 0
+ *     before its first kernel.
+ *   - Matrices are row-major.  h_pol, h_ref: [N x d]; W: [V x d] (the layout of
+ *     an nn.Linear weight), element type given by grpo_shape.dtype.  Every
+ *     matrix base pointer must be 16-byte aligned (the kernels read them with
+ *     the tensor memory accelerator).
+ *   - Row t = i*L + j is position j of completion i; completion i belongs to
+ *     prompt group i / G.  N = n_groups * G * L.
+ *   - All hidden-state rows, masked or not, must hold finite values.
+ *   - Nothing throws, aborts or exits the process.
+ */
+#ifndef GRPO_H
+#define GRPO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes (return values and the device `status` word) */
+enum {
+    GRPO_OK = 0,
+    GRPO_ERR_POINTER = 1,    /* null or misaligned pointer */
+    GRPO_ERR_SHAPE = 2,      /* bad shape or a token id outside [0, V) */
+    GRPO_ERR_WORKSPACE = 3,  /* workspace smaller than grpo_workspace_bytes() */
+    GRPO_ERR_LAUNCH = 4,     /* a CUDA launch or driver call failed */
+    GRPO_ERR_DTYPE = 5,      /* dtype not supported */
+    GRPO_ERR_TIMEOUT = 6,    /* a device-side wait ran out of time (kernel gave up, no hang) */
+    GRPO_ERR_DEVICE = 7      /* device is not sm_103 / lacks the needed shared memory */
+};
+
+typedef enum { GRPO_BF16 = 0, GRPO_FP16 = 1 } grpo_dtype;
+
+typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
+
+/* Problem description.
+ *   n_groups, G : prompts and completions per prompt (G >= 1)
+ *   L           : rows per completion (max completion length)
+ *   d           : hidden size, a multiple of 64
+ *   V           : vocabulary size (>= 1)
+ *   dtype       : storage/compute type of h_pol, h_ref, W (and of dH)
+ *   beta        : KL coefficient (0.04 in the pages' setting)
+ *   eps         : added to the group std in grpo_group_advantages
+ *   std_unbiased: 1 -> group std with divisor G-1, 0 -> divisor G
+ *   chunk_rows  : masked rows processed per backward chunk (0 -> 8192);
+ *                 rounded up to a multiple of 128. */
+typedef struct {
+    int n_groups, G, L, d, V;
+    grpo_dtype dtype;
+    float beta;
+    float eps;
+    int std_unbiased;
+    int chunk_rows;
+} grpo_shape;
+
+/* Fills a grpo_shape with the pages' defaults (beta 0.04, eps 1e-4, unbiased std). */
+void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, grpo_dtype dtype);
+
+/* Bytes of device workspace grpo_loss_fwd / grpo_loss_fwd_bwd need for this
+ * shape: O(chunk_rows * (V + d) + N), independent of how many rows are
+ * masked.  Returns 0 for an invalid shape. */
+size_t grpo_workspace_bytes(const grpo_shape* shape);
+
+/* Group-relative advantages ("Train your own R1 reasoning model with
+ * Unsloth", section 3, steps 3-5: score each response, take the group mean,
+ * compare every score with it).
+ *   rewards [n_groups*G] fp32 (device, read)    adv_out [n_groups*G] fp32 (device, written)
+ *   adv = (r - mean_group(r)) / (std_group(r) + eps), computed in fp64 with a
+ *   fixed summation order and rounded once to fp32 (bit-reproducible).
+ *   A group whose std divisor is 0 (G == 1 with std_unbiased) has std 0. */
+int grpo_group_advantages(const float* rewards, int n_groups, int G, float eps, int std_unbiased,
+                          float* adv_out, grpo_stream_t stream);
+
+/* Completion mask from completion lengths: mask[i*L + j] = (j < lengths[i]).
+ *   lengths [n_groups*G] int32 (device)   mask_out [N] uint8 (device, written) */
+int grpo_build_mask(const int32_t* lengths, const grpo_shape* shape, uint8_t* mask_out,
+                    grpo_stream_t stream);
+
+/* Indices of the masked-in rows in ascending order and their count.
+ *   mask [N] uint8 (device)   rows_out [N] int32 (device; first *n_valid entries written)
+ *   n_valid_out: one int32 (device).  workspace as for grpo_loss_fwd. */
+int grpo_valid_rows(const uint8_t* mask, const grpo_shape* shape, int32_t* rows_out,
+                    int32_t* n_valid_out, void* workspace, size_t ws_bytes, grpo_stream_t stream);
+
+/* Forward pass of the linear GRPO loss ("Long-context GRPO", section 2: the
+ * memory-efficient linear algorithm; section 4: the objective, the detach
+ * factor and the logsumexp trick).
+ *   h_pol, h_ref [N x d], W [V x d]          (dtype; device, read)
+ *   tokens [N] int32 in [0, V)               (device, read; masked rows too)
+ *   mask [N] uint8, nonzero = completion token (device, read)
+ *   adv [n_groups*G] fp32, one per completion (device, read)
+ *   workspace: >= grpo_workspace_bytes(shape) bytes of device memory, 256-byte aligned
+ *   loss_out: one fp32 (device) <- mean of ell_t over masked rows (0 if none)
+ *   row_stats: NULL or [N x 5] fp32 (device) <- (lse_pol, lse_ref, q, p, kl)
+ *              per row; zeros on masked rows
+ *   status: one int32 (device) <- 0 or an error code
+ * The result is bitwise reproducible from run to run. */
+int grpo_loss_fwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                  const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                  void* workspace, size_t ws_bytes, float* loss_out, float* row_stats,
+                  int32_t* status, grpo_stream_t stream);
+
+/* Forward and backward.  Same inputs and outputs as grpo_loss_fwd, plus
+ *   loss_scale: gradients are multiplied by it (1 for bf16; the fp16 loss
+ *               scale otherwise -- "Long-context GRPO", section 3: mixed
+ *               precision with automatic loss scaling breaks a naive linear
+ *               cross entropy unless handled)
+ *   dH [N x d] (dtype; device, written): loss_scale * d loss / d h_pol;
+ *               exactly 0 on masked rows
+ *   dW [V x d] fp32 (device, overwritten): loss_scale * d loss / d W
+ *   found_inf: one int32 (device) <- 1 if any scaled gradient value (the
+ *               16-bit dlogits, dH or dW) is not finite, else 0.  The caller
+ *               lowers the scale and calls again when it is set.
+ * The loss equals grpo_loss_fwd's bit for bit; dH and dW are bitwise
+ * reproducible (fixed reduction order, no floating-point atomics). */
+int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                      const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                      float loss_scale, void* workspace, size_t ws_bytes, float* loss_out,
+                      void* dH, float* dW, int32_t* found_inf, float* row_stats,
+                      int32_t* status, grpo_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* grpo_status_string(int status);
+
+/* Library version, as major*10000 + minor*100 + patch. */
+int grpo_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_H */

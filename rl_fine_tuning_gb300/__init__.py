@@ -1,0 +1,163 @@
+"""Python binding of libgrpo, the fused linear GRPO loss for GB300 (sm_103a).
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name in libgrpo.so, whose kernels do all the work.  Tensors are
+torch CUDA tensors (only their device pointers are passed); the stream
+defaults to torch's current stream.  A nonzero return code raises
+GrpoError.  There is no CPU fallback: importing the binding without the
+built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "GrpoError", "GrpoShape", "BF16", "FP16", "load", "make_shape", "grpo_workspace_bytes",
+    "grpo_group_advantages", "grpo_build_mask", "grpo_valid_rows", "grpo_loss_fwd", "grpo_loss_fwd_bwd",
+    "grpo_status_string", "grpo_version", "library_path",
+]
+
+BF16, FP16 = 0, 1
+
+
+class GrpoError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"libgrpo {what} failed: {code} ({_status_string(code)})")
+
+
+class GrpoShape(ctypes.Structure):
+    """Mirror of grpo_shape in include/grpo.h."""
+    _fields_ = [
+        ("n_groups", ctypes.c_int), ("G", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
+        ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
+        ("std_unbiased", ctypes.c_int), ("chunk_rows", ctypes.c_int),
+    ]
+
+    @property
+    def N(self) -> int:
+        return self.n_groups * self.G * self.L
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """The loaded libgrpo.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libgrpo.so is not built ({path}); run `python -m rl_fine_tuning_gb300.build`")
+    lib = ctypes.CDLL(path)
+    p, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    sp = ctypes.POINTER(GrpoShape)
+    lib.grpo_shape_init.argtypes = [sp, i32, i32, i32, i32, i32, i32]
+    lib.grpo_shape_init.restype = None
+    lib.grpo_workspace_bytes.argtypes = [sp]
+    lib.grpo_workspace_bytes.restype = sz
+    lib.grpo_group_advantages.argtypes = [p, i32, i32, f32, i32, p, p]
+    lib.grpo_build_mask.argtypes = [p, sp, p, p]
+    lib.grpo_valid_rows.argtypes = [p, sp, p, p, p, sz, p]
+    lib.grpo_loss_fwd.argtypes = [p, p, p, p, p, p, sp, p, sz, p, p, p, p]
+    lib.grpo_loss_fwd_bwd.argtypes = [p, p, p, p, p, p, sp, f32, p, sz, p, p, p, p, p, p, p]
+    lib.grpo_status_string.argtypes = [i32]
+    lib.grpo_status_string.restype = ctypes.c_char_p
+    lib.grpo_version.restype = i32
+    for name in ("grpo_group_advantages", "grpo_build_mask", "grpo_valid_rows", "grpo_loss_fwd",
+                 "grpo_loss_fwd_bwd"):
+        getattr(lib, name).restype = i32
+    _lib = lib
+    return lib
+
+
+def _status_string(code: int) -> str:
+    try:
+        return load().grpo_status_string(int(code)).decode()
+    except Exception:
+        return "?"
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return ctypes.c_void_p(x)
+    return ctypes.c_void_p(x.data_ptr())
+
+
+def _nbytes(x) -> int:
+    return x.numel() * x.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise GrpoError(code, what)
+
+
+def make_shape(n_groups, G, L, d, V, dtype=BF16, beta=0.04, eps=1e-4, std_unbiased=True, chunk_rows=0):
+    s = GrpoShape()
+    load().grpo_shape_init(ctypes.byref(s), n_groups, G, L, d, V, dtype)
+    s.beta, s.eps, s.std_unbiased, s.chunk_rows = beta, eps, int(bool(std_unbiased)), chunk_rows
+    return s
+
+
+def grpo_workspace_bytes(shape: GrpoShape) -> int:
+    return int(load().grpo_workspace_bytes(ctypes.byref(shape)))
+
+
+def grpo_group_advantages(rewards, n_groups, G, eps, std_unbiased, adv_out, stream=None):
+    _check(load().grpo_group_advantages(_ptr(rewards), n_groups, G, eps, int(bool(std_unbiased)), _ptr(adv_out),
+                                        _stream(stream)), "grpo_group_advantages")
+
+
+def grpo_build_mask(lengths, shape, mask_out, stream=None):
+    _check(load().grpo_build_mask(_ptr(lengths), ctypes.byref(shape), _ptr(mask_out), _stream(stream)),
+           "grpo_build_mask")
+
+
+def grpo_valid_rows(mask, shape, rows_out, n_valid_out, workspace, stream=None):
+    _check(load().grpo_valid_rows(_ptr(mask), ctypes.byref(shape), _ptr(rows_out), _ptr(n_valid_out),
+                                  _ptr(workspace), _nbytes(workspace), _stream(stream)), "grpo_valid_rows")
+
+
+def grpo_loss_fwd(h_pol, h_ref, W, tokens, mask, adv, shape, workspace, loss_out, row_stats, status,
+                  stream=None):
+    _check(load().grpo_loss_fwd(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv),
+                                ctypes.byref(shape), _ptr(workspace), _nbytes(workspace), _ptr(loss_out),
+                                _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd")
+
+
+def grpo_loss_fwd_bwd(h_pol, h_ref, W, tokens, mask, adv, shape, loss_scale, workspace, loss_out, dH, dW,
+                      found_inf, row_stats, status, stream=None):
+    _check(load().grpo_loss_fwd_bwd(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv),
+                                    ctypes.byref(shape), float(loss_scale), _ptr(workspace), _nbytes(workspace),
+                                    _ptr(loss_out), _ptr(dH), _ptr(dW), _ptr(found_inf), _ptr(row_stats),
+                                    _ptr(status), _stream(stream)), "grpo_loss_fwd_bwd")
+
+
+def grpo_status_string(code: int) -> str:
+    return _status_string(code)
+
+
+def grpo_version() -> int:
+    return int(load().grpo_version())

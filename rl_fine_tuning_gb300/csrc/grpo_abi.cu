@@ -1,0 +1,353 @@
+// C ABI of libgrpo: argument validation, workspace layout, TMA descriptors and
+// the launch sequence of the fused linear GRPO loss.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace grpo {
+
+namespace {
+
+constexpr int kVersion = 100;   // 0.1.0
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool shape_ok(const grpo_shape& s) {
+    if (s.n_groups < 1 || s.G < 1 || s.L < 1 || s.V < 1 || s.d < 64 || s.d % 64 != 0) return false;
+    if (s.d > 65536 || s.V > (1 << 30)) return false;
+    const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
+    if (N > (1LL << 31) - (1LL << 16)) return false;
+    if (s.chunk_rows < 0) return false;
+    return true;
+}
+
+bool dtype_ok(const grpo_shape& s) { return s.dtype == GRPO_BF16 || s.dtype == GRPO_FP16; }
+
+template <class P>
+bool aligned(const P* p, size_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+struct DeviceInfo {
+    int sm_count = 0;
+    bool ok = false;
+};
+
+int device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    int major = 0, minor = 0, smc = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smc, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (major != 10 || minor != 3) return GRPO_ERR_DEVICE;
+    if (smem < 200 * 1024) return GRPO_ERR_DEVICE;
+    out->sm_count = smc;
+    out->ok = true;
+    return GRPO_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D row-major matrix [rows x cols] of 16-bit elements with row pitch `pitch`
+// elements, 128-byte swizzled boxes of box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint64_t rows, uint64_t pitch,
+              uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int chunk_rows_of(const grpo_shape& s) {
+    int r = s.chunk_rows > 0 ? s.chunk_rows : kDefaultChunkRows;
+    r = (r + kBM - 1) / kBM * kBM;
+    const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
+    const int64_t nmax = (N + kBM - 1) / kBM * kBM;
+    if (r > nmax) r = static_cast<int>(nmax);
+    return r;
+}
+
+}  // namespace
+
+bool ws_layout(const grpo_shape& s, WsLayout* o) {
+    if (!shape_ok(s)) return false;
+    const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
+    o->N = N;
+    o->n_ntiles = (s.V + kBN - 1) / kBN;
+    int S = o->n_ntiles < kMaxFwdSplits ? o->n_ntiles : kMaxFwdSplits;
+    o->nps = (o->n_ntiles + S - 1) / S;
+    o->S = (o->n_ntiles + o->nps - 1) / o->nps;   // no empty split
+    o->R = chunk_rows_of(s);
+    o->V_pad = (s.V + 63) / 64 * 64;
+    o->nblk = static_cast<int>((N + kMergeThreads - 1) / kMergeThreads);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    o->counts = take(C_COUNT_WORDS * 4);
+    o->tiles = take(static_cast<size_t>(N) * 8);
+    o->rows = take(static_cast<size_t>(N) * 4);
+    o->part = take(static_cast<size_t>(N) * o->S * 16);
+    o->zt = take(static_cast<size_t>(N) * 8);
+    o->lse = take(static_cast<size_t>(N) * 4);
+    o->gco = take(static_cast<size_t>(N) * 4);
+    o->blocksum = take(static_cast<size_t>(o->nblk) * 8);
+    o->hc = take(static_cast<size_t>(o->R) * s.d * 2);
+    o->ds = take(static_cast<size_t>(o->R) * o->V_pad * 2);
+    o->total = off;
+    return true;
+}
+
+}  // namespace grpo
+
+using namespace grpo;
+
+namespace {
+
+struct Inputs {
+    const void *h_pol, *h_ref, *W;
+    const int32_t* tokens;
+    const uint8_t* mask;
+    const float* adv;
+    const grpo_shape* shape;
+    void* ws;
+    size_t ws_bytes;
+    float* loss_out;
+    float* row_stats;
+    int32_t* status;
+};
+
+int validate(const Inputs& in, WsLayout* L) {
+    if (!in.shape) return GRPO_ERR_SHAPE;
+    const grpo_shape& s = *in.shape;
+    if (!dtype_ok(s)) return GRPO_ERR_DTYPE;
+    if (!ws_layout(s, L)) return GRPO_ERR_SHAPE;
+    if (!in.h_pol || !in.h_ref || !in.W || !in.tokens || !in.mask || !in.adv || !in.ws || !in.loss_out ||
+        !in.status)
+        return GRPO_ERR_POINTER;
+    if (!aligned(in.h_pol, 16) || !aligned(in.h_ref, 16) || !aligned(in.W, 16) || !aligned(in.tokens, 4) ||
+        !aligned(in.adv, 4) || !aligned(in.ws, 256) || !aligned(in.loss_out, 4) || !aligned(in.status, 4) ||
+        (in.row_stats && !aligned(in.row_stats, 4)))
+        return GRPO_ERR_POINTER;
+    if (in.ws_bytes < L->total) return GRPO_ERR_WORKSPACE;
+    return GRPO_OK;
+}
+
+int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cudaStream_t st) {
+    const grpo_shape& s = *in.shape;
+    const bool bf16 = s.dtype == GRPO_BF16;
+    char* w = static_cast<char*>(in.ws);
+    int* counts = reinterpret_cast<int*>(w + L.counts);
+    cudaError_t e;
+    e = launch_index(in.mask, L.N, L.R, counts, reinterpret_cast<int*>(w + L.rows), reinterpret_cast<int2*>(w + L.tiles),
+                     in.status, nullptr, st);
+    if (e != cudaSuccess) return GRPO_ERR_LAUNCH;
+
+    CUtensorMap mHp, mHr, mW;
+    if (!make_map(&mHp, in.h_pol, bf16, s.d, L.N, s.d, kBK, kBM) ||
+        !make_map(&mHr, in.h_ref, bf16, s.d, L.N, s.d, kBK, kBM) ||
+        !make_map(&mW, in.W, bf16, s.d, s.V, s.d, kBK, kBN))
+        return GRPO_ERR_LAUNCH;
+    FwdParams fp;
+    fp.tiles = reinterpret_cast<const int2*>(w + L.tiles);
+    fp.counts = counts;
+    fp.tokens = in.tokens;
+    fp.part = reinterpret_cast<float4*>(w + L.part);
+    fp.zt = reinterpret_cast<float2*>(w + L.zt);
+    fp.V = s.V;
+    fp.d = s.d;
+    fp.S = L.S;
+    fp.nps = L.nps;
+    fp.n_ntiles = L.n_ntiles;
+    fp.status = in.status;
+    if (launch_fwd(fp, mHp, mHr, mW, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    if (launch_merge(L, w, in.mask, in.tokens, in.adv, s.L, s.V, s.beta, in.loss_out, in.row_stats, in.status, st) !=
+        cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    return GRPO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, grpo_dtype dtype) {
+    if (!s) return;
+    std::memset(s, 0, sizeof(*s));
+    s->n_groups = n_groups;
+    s->G = G;
+    s->L = L;
+    s->d = d;
+    s->V = V;
+    s->dtype = dtype;
+    s->beta = 0.04f;
+    s->eps = 1e-4f;
+    s->std_unbiased = 1;
+    s->chunk_rows = 0;
+}
+
+size_t grpo_workspace_bytes(const grpo_shape* shape) {
+    if (!shape) return 0;
+    WsLayout L;
+    if (!ws_layout(*shape, &L)) return 0;
+    return L.total;
+}
+
+int grpo_group_advantages(const float* rewards, int n_groups, int G, float eps, int std_unbiased, float* adv_out,
+                          grpo_stream_t stream) {
+    if (n_groups < 1 || G < 1) return GRPO_ERR_SHAPE;
+    if (!rewards || !adv_out || !aligned(rewards, 4) || !aligned(adv_out, 4)) return GRPO_ERR_POINTER;
+    return launch_advantages(rewards, n_groups, G, eps, std_unbiased, adv_out, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_LAUNCH;
+}
+
+int grpo_build_mask(const int32_t* lengths, const grpo_shape* shape, uint8_t* mask_out, grpo_stream_t stream) {
+    if (!shape || !shape_ok(*shape)) return GRPO_ERR_SHAPE;
+    if (!lengths || !mask_out || !aligned(lengths, 4)) return GRPO_ERR_POINTER;
+    return launch_build_mask(lengths, shape->n_groups * shape->G, shape->L, mask_out,
+                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_LAUNCH;
+}
+
+int grpo_valid_rows(const uint8_t* mask, const grpo_shape* shape, int32_t* rows_out, int32_t* n_valid_out,
+                    void* workspace, size_t ws_bytes, grpo_stream_t stream) {
+    if (!shape) return GRPO_ERR_SHAPE;
+    WsLayout L;
+    if (!ws_layout(*shape, &L)) return GRPO_ERR_SHAPE;
+    if (!mask || !rows_out || !n_valid_out || !workspace) return GRPO_ERR_POINTER;
+    if (!aligned(rows_out, 4) || !aligned(n_valid_out, 4) || !aligned(workspace, 256)) return GRPO_ERR_POINTER;
+    if (ws_bytes < L.total) return GRPO_ERR_WORKSPACE;
+    char* w = static_cast<char*>(workspace);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    int* counts = reinterpret_cast<int*>(w + L.counts);
+    int* scratch_status = counts + 8;
+    if (launch_index(mask, L.N, L.R, counts, rows_out, reinterpret_cast<int2*>(w + L.tiles), scratch_status, nullptr,
+                     st) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (cudaMemcpyAsync(n_valid_out, counts + C_NVALID, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    return GRPO_OK;
+}
+
+int grpo_loss_fwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens, const uint8_t* mask,
+                  const float* adv, const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out,
+                  float* row_stats, int32_t* status, grpo_stream_t stream) {
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, workspace, ws_bytes, loss_out, row_stats, status};
+    WsLayout L;
+    int rc = validate(in, &L);
+    if (rc != GRPO_OK) return rc;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    return run_forward(in, L, dev, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens, const uint8_t* mask,
+                      const float* adv, const grpo_shape* shape, float loss_scale, void* workspace, size_t ws_bytes,
+                      float* loss_out, void* dH, float* dW, int32_t* found_inf, float* row_stats, int32_t* status,
+                      grpo_stream_t stream) {
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, workspace, ws_bytes, loss_out, row_stats, status};
+    WsLayout L;
+    int rc = validate(in, &L);
+    if (rc != GRPO_OK) return rc;
+    if (!dH || !dW || !found_inf || !aligned(dH, 16) || !aligned(dW, 16) || !aligned(found_inf, 4))
+        return GRPO_ERR_POINTER;
+    if (!(loss_scale > 0.f) || !std::isfinite(loss_scale)) return GRPO_ERR_SHAPE;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const grpo_shape& s = *shape;
+    const bool bf16 = s.dtype == GRPO_BF16;
+    char* w = static_cast<char*>(workspace);
+    int* counts = reinterpret_cast<int*>(w + L.counts);
+
+    rc = run_forward(in, L, dev, st);
+    if (rc != GRPO_OK) return rc;
+
+    // zero the reported overflow flag and the masked rows of dH; dW when nothing is masked in
+    if (launch_clear_grads(counts, found_inf, dW, static_cast<int64_t>(s.V) * s.d, st) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (launch_zero_masked_rows(mask, L.N, s.d, dH, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+
+    CUtensorMap mW_k, mW_mn, mHc_k, mHc_mn, mDS_k, mDS_mn;
+    void* hc = w + L.hc;
+    void* ds = w + L.ds;
+    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN) || !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) ||
+        !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) || !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
+        !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
+        !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK))
+        return GRPO_ERR_LAUNCH;
+
+    ChunkParams cp;
+    cp.counts = counts;
+    cp.rows = reinterpret_cast<const int*>(w + L.rows);
+    cp.tokens = tokens;
+    cp.lse = reinterpret_cast<const float*>(w + L.lse);
+    cp.gco = reinterpret_cast<const float*>(w + L.gco);
+    cp.scale = loss_scale;
+    cp.V = s.V;
+    cp.d = s.d;
+    cp.V_pad = L.V_pad;
+    cp.dS = static_cast<uint16_t*>(ds);
+    cp.dH = static_cast<uint16_t*>(dH);
+    cp.dW = dW;
+    cp.found_inf = found_inf;
+    cp.status = status;
+    const int64_t max_chunks = (L.N + L.R - 1) / L.R;
+    for (int64_t c = 0; c < max_chunks; ++c) {
+        cp.chunk = static_cast<int>(c);
+        if (launch_gather_rows(cp, h_pol, hc, L.R, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+        if (launch_ds(cp, mHc_k, mW_k, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+        if (launch_dh(cp, mDS_k, mW_mn, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+        if (launch_dw(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    }
+    return GRPO_OK;
+}
+
+const char* grpo_status_string(int status) {
+    switch (status) {
+        case GRPO_OK: return "ok";
+        case GRPO_ERR_POINTER: return "null or misaligned pointer";
+        case GRPO_ERR_SHAPE: return "bad shape or token id";
+        case GRPO_ERR_WORKSPACE: return "workspace too small";
+        case GRPO_ERR_LAUNCH: return "CUDA launch or driver error";
+        case GRPO_ERR_DTYPE: return "unsupported dtype";
+        case GRPO_ERR_TIMEOUT: return "device wait timed out";
+        case GRPO_ERR_DEVICE: return "device is not an sm_103 GPU with enough shared memory";
+        default: return "unknown status";
+    }
+}
+
+int grpo_version(void) { return kVersion; }
+
+}  // extern "C"

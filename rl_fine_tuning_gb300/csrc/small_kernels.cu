@@ -1,0 +1,391 @@
+// Bandwidth-light steps of the GRPO loss: advantages, mask / row index,
+// logsumexp merge + objective + deterministic loss, row gather and zeroing.
+#include <cfloat>
+#include <cmath>
+
+#include "internal.h"
+
+namespace grpo {
+
+// ------------------------------------------------------------ advantages
+// Group-relative advantage, fp64 with a fixed summation order and explicit
+// round-to-nearest operations (no contraction), so the result is the same
+// bit pattern on every run ("Train your own R1 reasoning model with Unsloth",
+// section 3: score, group mean, compare each score with it).
+__global__ void k_advantages(const float* __restrict__ r, int n_groups, int G, float eps, int std_unbiased,
+                             float* __restrict__ adv) {
+    const int gi = blockIdx.x * blockDim.x + threadIdx.x;
+    if (gi >= n_groups) return;
+    const float* rr = r + static_cast<size_t>(gi) * G;
+    double sum = 0.0;
+    for (int i = 0; i < G; ++i) sum = __dadd_rn(sum, static_cast<double>(rr[i]));
+    const double mu = __ddiv_rn(sum, static_cast<double>(G));
+    double ss = 0.0;
+    for (int i = 0; i < G; ++i) {
+        const double dv = __dsub_rn(static_cast<double>(rr[i]), mu);
+        ss = __dadd_rn(ss, __dmul_rn(dv, dv));
+    }
+    const int div = std_unbiased ? G - 1 : G;
+    const double sigma = div > 0 ? __dsqrt_rn(__ddiv_rn(ss, static_cast<double>(div))) : 0.0;
+    const double den = __dadd_rn(sigma, static_cast<double>(eps));
+    for (int i = 0; i < G; ++i)
+        adv[static_cast<size_t>(gi) * G + i] =
+            __double2float_rn(__ddiv_rn(__dsub_rn(static_cast<double>(rr[i]), mu), den));
+}
+
+cudaError_t launch_advantages(const float* r, int n_groups, int G, float eps, int std_unbiased, float* adv,
+                              cudaStream_t st) {
+    const int thr = 128;
+    k_advantages<<<(n_groups + thr - 1) / thr, thr, 0, st>>>(r, n_groups, G, eps, std_unbiased, adv);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ mask
+__global__ void k_build_mask(const int32_t* __restrict__ lengths, int n_seq, int L, uint8_t* __restrict__ mask) {
+    const int64_t n = static_cast<int64_t>(n_seq) * L;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < n;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(t / L);
+        const int j = static_cast<int>(t - static_cast<int64_t>(i) * L);
+        mask[t] = static_cast<uint8_t>(j < lengths[i]);
+    }
+}
+
+cudaError_t launch_build_mask(const int32_t* lengths, int n_seq, int L, uint8_t* mask, cudaStream_t st) {
+    const int64_t n = static_cast<int64_t>(n_seq) * L;
+    int blocks = static_cast<int>((n + 255) / 256);
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    k_build_mask<<<blocks, 256, 0, st>>>(lengths, n_seq, L, mask);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ row index
+// One block walks the mask in segments of kIndexThreads*kItems rows, carrying
+// the running counts between segments.  Outputs, all in ascending row order:
+//   rows[]  -- every masked-in row
+//   tiles[] -- forward row tiles: runs of consecutive masked-in rows cut into
+//              pieces of at most kBM rows (first row, row count)
+// and the chunking of the backward pass over the valid-row list.
+constexpr int kItems = 16;
+
+__device__ __forceinline__ int block_excl_sum(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int y = lane < nw ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y += z;
+        }
+        if (lane < nw) s_warp[lane] = y;
+    }
+    __syncthreads();
+    const int off = w > 0 ? s_warp[w - 1] : 0;
+    *total = s_warp[nw - 1];
+    __syncthreads();
+    return off + x - v;
+}
+
+__device__ __forceinline__ int block_excl_max(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x = max(x, y);
+    }
+    int excl_in_warp = __shfl_up_sync(0xffffffffu, x, 1);
+    if (lane == 0) excl_in_warp = -1;
+    if (lane == 31) s_warp[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int y = lane < nw ? s_warp[lane] : -1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y = max(y, z);
+        }
+        if (lane < nw) s_warp[lane] = y;
+    }
+    __syncthreads();
+    const int off = w > 0 ? s_warp[w - 1] : -1;
+    *total = s_warp[nw - 1];
+    __syncthreads();
+    return max(off, excl_in_warp);
+}
+
+__global__ void __launch_bounds__(kIndexThreads) k_index(const uint8_t* __restrict__ mask, int64_t N, int R_max,
+                                                         int* __restrict__ counts, int* __restrict__ rows,
+                                                         int2* __restrict__ tiles, int* status, int* found_inf) {
+    __shared__ int s_warp[32];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        *status = 0;
+        if (found_inf) *found_inf = 0;
+    }
+    int carry_valid = 0, carry_tiles = 0, carry_lastzero = -1;
+    for (int64_t base = 0; base < N; base += static_cast<int64_t>(kIndexThreads) * kItems) {
+        const int t0 = static_cast<int>(base) + tid * kItems;
+        uint32_t bits = 0;
+#pragma unroll
+        for (int k = 0; k < kItems; ++k) {
+            const int64_t t = static_cast<int64_t>(t0) + k;
+            if (t < N && mask[t] != 0) bits |= 1u << k;
+        }
+        int nv = __popc(bits);
+        int lz = -1;
+#pragma unroll
+        for (int k = 0; k < kItems; ++k)
+            if (!((bits >> k) & 1u)) lz = t0 + k;
+        int tot_nv, tot_lz, tot_ns;
+        const int nv_excl = block_excl_sum(nv, s_warp, &tot_nv);
+        const int lz_excl = block_excl_max(lz, s_warp, &tot_lz);
+        const int last_zero = max(carry_lastzero, lz_excl);
+        int ns = 0;
+        {
+            int lzr = last_zero;
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                if (!((bits >> k) & 1u)) {
+                    lzr = t0 + k;
+                } else if ((((t0 + k) - lzr - 1) & (kBM - 1)) == 0) {
+                    ++ns;
+                }
+            }
+        }
+        const int ns_excl = block_excl_sum(ns, s_warp, &tot_ns);
+        {
+            int vi = carry_valid + nv_excl, ti = carry_tiles + ns_excl, lzr = last_zero;
+#pragma unroll
+            for (int k = 0; k < kItems; ++k) {
+                const int t = t0 + k;
+                if (!((bits >> k) & 1u)) {
+                    lzr = t;
+                } else {
+                    rows[vi++] = t;
+                    if (((t - lzr - 1) & (kBM - 1)) == 0) tiles[ti++] = make_int2(t, 0);
+                }
+            }
+        }
+        carry_valid += tot_nv;
+        carry_tiles += tot_ns;
+        carry_lastzero = max(carry_lastzero, tot_lz);
+    }
+    if (tid == 0) {
+        const int nv = carry_valid;
+        const int n_chunks = nv > 0 ? (nv + R_max - 1) / R_max : 0;
+        int rc = 0;
+        if (n_chunks > 0) {
+            rc = (nv + n_chunks - 1) / n_chunks;
+            rc = (rc + kBM - 1) / kBM * kBM;
+        }
+        counts[C_NVALID] = nv;
+        counts[C_NTILES] = carry_tiles;
+        counts[C_NCHUNKS] = n_chunks;
+        counts[C_CHUNK_ROWS] = rc;
+        counts[C_WINV] = __float_as_int(1.0f / static_cast<float>(nv > 0 ? nv : 1));
+    }
+}
+
+// rows covered by each forward tile: up to kBM, stopping at the end of the run
+__global__ void k_tile_rows(const uint8_t* __restrict__ mask, int64_t N, const int* __restrict__ counts,
+                            int2* __restrict__ tiles) {
+    const int n_tiles = counts[C_NTILES];
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_tiles; i += gridDim.x * blockDim.x) {
+        const int t0 = tiles[i].x;
+        int n = 1;
+        while (n < kBM && static_cast<int64_t>(t0) + n < N && mask[t0 + n] != 0) ++n;
+        tiles[i].y = n;
+    }
+}
+
+cudaError_t launch_index(const uint8_t* mask, int64_t N, int R_max, int* counts, int* rows, int2* tiles,
+                         int* status, int* found_inf, cudaStream_t st) {
+    k_index<<<1, kIndexThreads, 0, st>>>(mask, N, R_max, counts, rows, tiles, status, found_inf);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int blocks = static_cast<int>((N / kBM + 255) / 256) + 1;
+    if (blocks > 1024) blocks = 1024;
+    k_tile_rows<<<blocks, 256, 0, st>>>(mask, N, counts, tiles);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ merge + objective
+// Per row: merge the per-split (max, sum-exp) partials of the policy and the
+// reference logits into their logsumexp, form q, p, the reverse-KL term
+// exp(p-q) - (p-q) - 1 = expm1(x) - x, the per-token objective and its
+// derivative w.r.t. q ("Long-context GRPO", section 4).  The masked sum of the
+// objective is reduced in fp64 along a fixed tree.
+__device__ __forceinline__ float merge_lse(const float4* __restrict__ part, int S, bool ref) {
+    float m = -INFINITY;
+    for (int s = 0; s < S; ++s) m = fmaxf(m, ref ? part[s].z : part[s].x);
+    float acc = 0.f;
+    for (int s = 0; s < S; ++s) {
+        const float ms = ref ? part[s].z : part[s].x;
+        const float ss = ref ? part[s].w : part[s].y;
+        acc += ss * expf(ms - m);
+    }
+    return m + logf(acc);
+}
+
+__global__ void __launch_bounds__(kMergeThreads) k_merge(const float4* __restrict__ part, const float2* __restrict__ zt,
+                                                         int S, const uint8_t* __restrict__ mask,
+                                                         const int* __restrict__ tokens, const float* __restrict__ adv,
+                                                         int L, int V, float beta, int64_t N, float* __restrict__ lse_out,
+                                                         float* __restrict__ g_out, double* __restrict__ blocksum,
+                                                         float* __restrict__ row_stats, int* status) {
+    __shared__ double sh[kMergeThreads];
+    const int64_t t = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
+    double ell = 0.0;
+    if (t < N) {
+        float lse_p = 0.f, lse_r = 0.f, q = 0.f, p = 0.f, kl = 0.f, g = 0.f;
+        if (mask[t]) {
+            const int tok = tokens[t];
+            if (tok < 0 || tok >= V) {
+                atomicCAS(status, 0, GRPO_ERR_SHAPE);
+            } else {
+                const float4* pr = part + t * S;
+                lse_p = merge_lse(pr, S, false);
+                lse_r = merge_lse(pr, S, true);
+                const float2 z = zt[t];
+                q = z.x - lse_p;
+                p = z.y - lse_r;
+                const float x = p - q;
+                const float em1 = expm1f(x);
+                kl = em1 - x;
+                const float A = adv[t / L];
+                ell = static_cast<double>(-A + beta * kl);
+                g = -A - beta * em1;
+            }
+        }
+        lse_out[t] = lse_p;
+        g_out[t] = g;
+        if (row_stats) {
+            float* o = row_stats + t * 5;
+            o[0] = lse_p;
+            o[1] = lse_r;
+            o[2] = q;
+            o[3] = p;
+            o[4] = kl;
+        }
+    }
+    sh[threadIdx.x] = ell;
+    __syncthreads();
+#pragma unroll
+    for (int s = kMergeThreads / 2; s > 0; s >>= 1) {
+        if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) blocksum[blockIdx.x] = sh[0];
+}
+
+__global__ void __launch_bounds__(1024) k_loss_final(const double* __restrict__ blocksum, int nblk,
+                                                     const int* __restrict__ counts, float* __restrict__ loss_out) {
+    __shared__ double sh[1024];
+    double acc = 0.0;
+    for (int i = threadIdx.x; i < nblk; i += 1024) acc += blocksum[i];
+    sh[threadIdx.x] = acc;
+    __syncthreads();
+    for (int s = 512; s > 0; s >>= 1) {
+        if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        const int nv = counts[C_NVALID];
+        *loss_out = nv > 0 ? static_cast<float>(sh[0] / static_cast<double>(nv)) : 0.f;
+    }
+}
+
+cudaError_t launch_merge(const WsLayout& ws, char* wsp, const uint8_t* mask, const int* tokens, const float* adv,
+                         int L, int V, float beta, float* loss_out, float* row_stats, int* status,
+                         cudaStream_t st) {
+    k_merge<<<ws.nblk, kMergeThreads, 0, st>>>(
+        reinterpret_cast<const float4*>(wsp + ws.part), reinterpret_cast<const float2*>(wsp + ws.zt), ws.S, mask,
+        tokens, adv, L, V, beta, ws.N, reinterpret_cast<float*>(wsp + ws.lse), reinterpret_cast<float*>(wsp + ws.gco),
+        reinterpret_cast<double*>(wsp + ws.blocksum), row_stats, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<const double*>(wsp + ws.blocksum), ws.nblk,
+                                     reinterpret_cast<const int*>(wsp + ws.counts), loss_out);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ gather / zero
+// Hc[slot] = h_pol[rows[c0 + slot]] for the chunk's slots; the slots after
+// the last one, up to the next multiple of kBM, are zeroed.
+__global__ void k_gather_rows(const int* __restrict__ counts, const int* __restrict__ rows, int chunk,
+                              const uint4* __restrict__ h, uint4* __restrict__ hc, int vec_per_row, int R) {
+    if (chunk >= counts[C_NCHUNKS]) return;
+    const int rc = counts[C_CHUNK_ROWS];
+    const int c0 = chunk * rc;
+    const int n_c = min(rc, counts[C_NVALID] - c0);
+    const int n_fill = min(R, (n_c + kBM - 1) / kBM * kBM);
+    const int64_t total = static_cast<int64_t>(n_fill) * vec_per_row;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int slot = static_cast<int>(i / vec_per_row);
+        const int v = static_cast<int>(i - static_cast<int64_t>(slot) * vec_per_row);
+        uint4 x = make_uint4(0, 0, 0, 0);
+        if (slot < n_c) x = h[static_cast<int64_t>(rows[c0 + slot]) * vec_per_row + v];
+        hc[i] = x;
+    }
+}
+
+cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, int R, cudaStream_t st) {
+    const int vpr = p.d / 8;
+    const int64_t total = static_cast<int64_t>(R) * vpr;
+    int blocks = static_cast<int>((total + 255) / 256);
+    if (blocks > 148 * 16) blocks = 148 * 16;
+    k_gather_rows<<<blocks, 256, 0, st>>>(p.counts, p.rows, p.chunk, static_cast<const uint4*>(h_pol),
+                                          static_cast<uint4*>(hc), vpr, R);
+    return cudaGetLastError();
+}
+
+__global__ void k_zero_masked_rows(const uint8_t* __restrict__ mask, int64_t N, int vec_per_row,
+                                   uint4* __restrict__ dH) {
+    const int64_t total = N * vec_per_row;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / vec_per_row;
+        if (!mask[t]) dH[i] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st) {
+    const int vpr = d / 8;
+    const int64_t total = N * vpr;
+    int blocks = static_cast<int>((total + 255) / 256);
+    if (blocks > 148 * 16) blocks = 148 * 16;
+    if (blocks < 1) blocks = 1;
+    k_zero_masked_rows<<<blocks, 256, 0, st>>>(mask, N, vpr, static_cast<uint4*>(dH));
+    return cudaGetLastError();
+}
+
+// found_inf <- 0; dW <- 0 when no row is masked in (no backward chunk runs then)
+__global__ void k_clear_grads(const int* __restrict__ counts, int* found_inf, float4* __restrict__ dW, int64_t n4) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) *found_inf = 0;
+    if (counts[C_NVALID] != 0) return;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        dW[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, cudaStream_t st) {
+    const int64_t n4 = n / 4;
+    int blocks = static_cast<int>((n4 + 255) / 256);
+    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks < 1) blocks = 1;
+    k_clear_grads<<<blocks, 256, 0, st>>>(counts, found_inf, reinterpret_cast<float4*>(dW), n4);
+    return cudaGetLastError();
+}
+
+}  // namespace grpo

@@ -1,0 +1,649 @@
+// Tensor-core kernels of the linear GRPO loss (tcgen05 + TMEM, fed by TMA).
+//
+//   fwd : z = H . W^T for the policy and the reference rows of one row tile,
+//         both MMAs reading the same W stage; the epilogue keeps a running
+//         (max, sum exp) per row and picks out z[tok] -- the logits are never
+//         written anywhere ("Long-context GRPO", section 2: the linear
+//         algorithm; section 4: the logsumexp trick).
+//   ds  : recomputes the policy logits of a chunk of valid rows and writes
+//         the scaled dlogits  s * g_t * (onehot(tok_t) - softmax(z_t))  as
+//         16-bit values into the chunk buffer.
+//   dh  : dH[rows] = (1/N_valid) * dlogits . W        (K = vocabulary)
+//   dw  : dW      += (1/N_valid) * dlogits^T . H_pol  (K = chunk rows)
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warps 2..5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31,
+//               i.e. one accumulator row per thread.
+// Stages: smem ring of kStages K-slices (64 elements = one 128-byte swizzle
+// span), full/empty mbarriers; accumulators: kAccBufs TMEM buffers with
+// acc_full/acc_empty mbarriers so the epilogue of one tile overlaps the MMAs
+// of the next.
+#include <cmath>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace grpo {
+
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Operand layouts in shared memory (all 128-byte swizzled, as TMA writes them
+// with CU_TENSOR_MAP_SWIZZLE_128B):
+//   K-major  [rows][64 K-elements]: row r at r*128 B; 8-row groups 1024 B apart
+//            (SBO = 1024).  K sub-step kk (16 elements) = +32 B.
+//   MN-major [64 K-rows][64 MN-elements] boxes of 8 KB; box j holds MN
+//            elements 64j..64j+63 (LBO = 8192); 8-K-row groups 1024 B apart
+//            (SBO = 1024).  K sub-step kk = +2048 B.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t a) { return make_sdesc_sw128(a, 16, 1024); }
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t a) { return make_sdesc_sw128(a, 8192, 1024); }
+
+struct Smem {
+    uint8_t* stages;
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* acc_full;
+    uint64_t* acc_empty;
+    uint64_t* drain;
+    uint32_t* tmem_slot;
+    volatile int* abort_flag;
+};
+
+template <int kStages, int kStageBytes>
+__device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
+    Smem s;
+    const uint32_t a = smem_u32(raw);
+    uint8_t* base = raw + ((1024u - (a & 1023u)) & 1023u);
+    s.stages = base;
+    s.full = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
+    s.empty = s.full + kStages;
+    s.acc_full = s.empty + kStages;
+    s.acc_empty = s.acc_full + 2;
+    s.drain = s.acc_empty + 2;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+    return s;
+}
+
+template <class T>
+constexpr int smem_bytes() {
+    return T::kStages * T::kStageBytes + 1024 + 256;
+}
+
+__device__ __forceinline__ uint16_t f32_to_16(float x, bool bf16) {
+    if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    return __half_as_ushort(__float2half_rn(x));
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
+    return static_cast<uint32_t>(f32_to_16(a, bf16)) | (static_cast<uint32_t>(f32_to_16(b, bf16)) << 16);
+}
+
+// non-finite check of a packed pair of fp16 values (exponent all ones)
+__device__ __forceinline__ bool half2_nonfinite(uint32_t u) {
+    return ((u & 0x7C00u) == 0x7C00u) || ((u & 0x7C000000u) == 0x7C000000u);
+}
+
+// ====================================================================== traits
+// Each traits class describes one kernel: its schedule of work units, the TMA
+// loads of one K-stage, the MMAs of one K-stage and the epilogue.
+
+struct FwdT {
+    static constexpr int kStages = 3;
+    static constexpr int kStageBytes = 2 * 16384 + 32768;   // A_pol, A_ref (128x64), B (256x64)
+    static constexpr int kAccBufs = 1;
+    static constexpr int kAccStride = 0;
+    using Params = FwdParams;
+    struct Sched {
+        int n_units, ks;
+    };
+    struct Coord {
+        int t0, n0;
+    };
+    struct Epi {
+        float m[2], s[2], zt[2];
+        int tok, t, split;
+        bool valid, found;
+    };
+
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        sc.n_units = p.counts[C_NTILES] * p.S;
+        sc.ks = p.d / kBK;
+        return sc.n_units > 0;
+    }
+    __device__ static int items(const Params& p, const Sched&, int unit) {
+        const int s = unit % p.S;
+        const int nb = s * p.nps;
+        const int ne = min(nb + p.nps, p.n_ntiles);
+        return max(ne - nb, 0);
+    }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params& p, const Sched&, int unit, int item) {
+        Coord c;
+        c.t0 = p.tiles[unit / p.S].x;
+        c.n0 = ((unit % p.S) * p.nps + item) * kBN;
+        return c;
+    }
+    __device__ static uint32_t tx_bytes(const Params&, const Coord&) { return kStageBytes; }
+    __device__ static void load(const Params&, const Coord& c, int k, uint8_t* st, uint64_t* bar,
+                                const CUtensorMap* mA, const CUtensorMap* mA2, const CUtensorMap* mB) {
+        tma_load_2d(mA, bar, st, k * kBK, c.t0);
+        tma_load_2d(mA2, bar, st + 16384, k * kBK, c.t0);
+        tma_load_2d(mB, bar, st + 32768, k * kBK, c.n0);
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t b = desc_kmajor(st + 32768 + kk * 32);
+            const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+            umma_f16(acc, desc_kmajor(st + kk * 32), b, idesc, accum);
+            umma_f16(acc + 256, desc_kmajor(st + 16384 + kk * 32), b, idesc, accum);
+        }
+    }
+    __device__ static void epi_begin(const Params& p, const Sched&, int unit, int row, Epi& e) {
+        const int2 tile = p.tiles[unit / p.S];
+        e.t = tile.x + row;
+        e.valid = row < tile.y;
+        e.tok = e.valid ? p.tokens[e.t] : -1;
+        e.split = unit % p.S;
+        e.m[0] = e.m[1] = -INFINITY;
+        e.s[0] = e.s[1] = 0.f;
+        e.zt[0] = e.zt[1] = 0.f;
+        e.found = false;
+    }
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched&, int unit, int item, uint32_t tacc, Epi& e) {
+        const int n0 = ((unit % p.S) * p.nps + item) * kBN;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+#pragma unroll 1
+            for (int c = 0; c < kBN / 32; ++c) {
+                const int col0 = n0 + c * 32;
+                if (col0 >= p.V) break;
+                float v[32];
+                tmem_ld32(tacc + w * 256 + c * 32, v);
+                const int nvalid = p.V - col0;
+                if (nvalid < 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j >= nvalid) v[j] = -INFINITY;
+                }
+                float cmax = v[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+                const float m_new = fmaxf(e.m[w], cmax);
+                const float mb = m_new * kLog2e;
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc += fast_exp2(fmaf(v[j], kLog2e, -mb));
+                e.s[w] = fmaf(e.s[w], fast_exp2(fmaf(e.m[w], kLog2e, -mb)), acc);
+                e.m[w] = m_new;
+                const bool hit = static_cast<unsigned>(e.tok - col0) < 32u;
+                if (__any_sync(0xffffffffu, hit)) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (e.tok == col0 + j) e.zt[w] = v[j];
+                    if (hit) e.found = true;
+                }
+            }
+        }
+    }
+    __device__ static void epi_end(const Params& p, const Sched&, int, Epi& e) {
+        if (!e.valid) return;
+        p.part[static_cast<int64_t>(e.t) * p.S + e.split] = make_float4(e.m[0], e.s[0], e.m[1], e.s[1]);
+        if (e.found) p.zt[e.t] = make_float2(e.zt[0], e.zt[1]);
+    }
+};
+
+// chunk bookkeeping shared by the backward kernels
+struct ChunkSched {
+    int n_units, ks, c0, n_c, n_mt, n_nt;
+    float winv;
+};
+
+__device__ __forceinline__ bool chunk_setup(const ChunkParams& p, ChunkSched& sc) {
+    if (p.chunk >= p.counts[C_NCHUNKS]) return false;
+    const int rc = p.counts[C_CHUNK_ROWS];
+    sc.c0 = p.chunk * rc;
+    sc.n_c = min(rc, p.counts[C_NVALID] - sc.c0);
+    sc.n_mt = (sc.n_c + kBM - 1) / kBM;
+    sc.winv = __int_as_float(p.counts[C_WINV]);
+    return sc.n_c > 0;
+}
+
+struct DsT {
+    static constexpr int kStages = 4;
+    static constexpr int kStageBytes = 16384 + 32768;   // A (128x64), B (256x64)
+    static constexpr int kAccBufs = 2;
+    static constexpr int kAccStride = 256;
+    using Params = ChunkParams;
+    using Sched = ChunkSched;
+    struct Coord {
+        int m0, n0;
+    };
+    struct Epi {
+        int slot;
+    };
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!chunk_setup(p, sc)) return false;
+        sc.n_nt = (p.V + kBN - 1) / kBN;
+        sc.ks = p.d / kBK;
+        sc.n_units = sc.n_mt * sc.n_nt;
+        return true;
+    }
+    __device__ static int items(const Params&, const Sched&, int) { return 1; }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int) {
+        return Coord{(unit % sc.n_mt) * kBM, (unit / sc.n_mt) * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params&, const Coord&) { return kStageBytes; }
+    __device__ static void load(const Params&, const Coord& c, int k, uint8_t* st, uint64_t* bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB) {
+        tma_load_2d(mA, bar, st, k * kBK, c.m0);
+        tma_load_2d(mB, bar, st + 16384, k * kBK, c.n0);
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_f16(acc, desc_kmajor(st + kk * 32), desc_kmajor(st + 16384 + kk * 32), idesc,
+                     (first && kk == 0) ? 0u : 1u);
+    }
+    __device__ static void epi_begin(const Params&, const Sched&, int, int, Epi&) {}
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int slot = (unit % sc.n_mt) * kBM + row;
+        const int n0 = (unit / sc.n_mt) * kBN;
+        const bool valid = slot < sc.n_c;
+        int t = 0, tok = -1;
+        float coef = 0.f, lse2 = 0.f;
+        if (valid) {
+            t = p.rows[sc.c0 + slot];
+            tok = p.tokens[t];
+            coef = p.scale * p.gco[t];
+            lse2 = p.lse[t] * kLog2e;
+        }
+        uint16_t* out = p.dS + static_cast<int64_t>(slot) * p.V_pad;
+        bool bad = false;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.V) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float p0 = fast_exp2(fmaf(v[j], kLog2e, -lse2));
+                const float p1 = fast_exp2(fmaf(v[j + 1], kLog2e, -lse2));
+                const float d0 = coef * ((col0 + j == tok ? 1.f : 0.f) - p0);
+                const float d1 = coef * ((col0 + j + 1 == tok ? 1.f : 0.f) - p1);
+                pk[j / 2] = pack2(d0, d1, kBf16);
+            }
+            if (!kBf16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
+            }
+            if (col0 + 32 <= p.V) {
+                uint4* o4 = reinterpret_cast<uint4*>(out + col0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < p.V) out[col0 + j] = static_cast<uint16_t>((pk[j / 2] >> (16 * (j & 1))) & 0xFFFFu);
+            }
+        }
+        if (bad) atomicOr(p.found_inf, 1);
+    }
+    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
+};
+
+struct DhT {
+    static constexpr int kStages = 4;
+    static constexpr int kStageBytes = 16384 + 32768;   // A (128 slots x 64 vocab), B (64 vocab x 256 d)
+    static constexpr int kAccBufs = 2;
+    static constexpr int kAccStride = 256;
+    using Params = ChunkParams;
+    using Sched = ChunkSched;
+    struct Coord {
+        int m0, n0;
+    };
+    struct Epi {
+        int slot;
+    };
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!chunk_setup(p, sc)) return false;
+        sc.n_nt = (p.d + kBN - 1) / kBN;
+        sc.ks = (p.V + kBK - 1) / kBK;
+        sc.n_units = sc.n_mt * sc.n_nt;
+        return true;
+    }
+    __device__ static int items(const Params&, const Sched&, int) { return 1; }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int) {
+        return Coord{(unit / sc.n_nt) * kBM, (unit % sc.n_nt) * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Coord& c) {
+        return 16384 + 8192 * min(4, (p.d - c.n0) / 64);
+    }
+    __device__ static void load(const Params& p, const Coord& c, int k, uint8_t* st, uint64_t* bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB) {
+        tma_load_2d(mA, bar, st, k * kBK, c.m0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (c.n0 + 64 * j < p.d) tma_load_2d(mB, bar, st + 16384 + 8192 * j, c.n0 + 64 * j, k * kBK);
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_f16(acc, desc_kmajor(st + kk * 32), desc_mnmajor(st + 16384 + kk * 2048), idesc,
+                     (first && kk == 0) ? 0u : 1u);
+    }
+    __device__ static void epi_begin(const Params&, const Sched&, int, int, Epi&) {}
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int slot = (unit / sc.n_nt) * kBM + row;
+        const int n0 = (unit % sc.n_nt) * kBN;
+        const bool valid = slot < sc.n_c;
+        const int t = valid ? p.rows[sc.c0 + slot] : 0;
+        uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
+        bool bad = false;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2(v[j] * sc.winv, v[j + 1] * sc.winv, kBf16);
+            if (!kBf16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
+            }
+            if (valid) {
+                uint4* o4 = reinterpret_cast<uint4*>(out + col0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+        }
+        if (bad && valid) atomicOr(p.found_inf, 1);
+    }
+    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
+};
+
+struct DwT {
+    static constexpr int kStages = 4;
+    static constexpr int kStageBytes = 16384 + 32768;   // A (64 slots x 128 vocab), B (64 slots x 256 d)
+    static constexpr int kAccBufs = 2;
+    static constexpr int kAccStride = 256;
+    using Params = ChunkParams;
+    using Sched = ChunkSched;
+    struct Coord {
+        int v0, n0;
+    };
+    struct Epi {
+        int v;
+    };
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!chunk_setup(p, sc)) return false;
+        sc.n_nt = (p.d + kBN - 1) / kBN;
+        sc.ks = (sc.n_c + kBK - 1) / kBK;
+        sc.n_units = ((p.V + kBM - 1) / kBM) * sc.n_nt;
+        return true;
+    }
+    __device__ static int items(const Params&, const Sched&, int) { return 1; }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int) {
+        return Coord{(unit / sc.n_nt) * kBM, (unit % sc.n_nt) * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Coord& c) {
+        return 16384 + 8192 * min(4, (p.d - c.n0) / 64);
+    }
+    __device__ static void load(const Params& p, const Coord& c, int k, uint8_t* st, uint64_t* bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB) {
+        tma_load_2d(mA, bar, st, c.v0, k * kBK);
+        tma_load_2d(mA, bar, st + 8192, c.v0 + 64, k * kBK);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (c.n0 + 64 * j < p.d) tma_load_2d(mB, bar, st + 16384 + 8192 * j, c.n0 + 64 * j, k * kBK);
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_f16(acc, desc_mnmajor(st + kk * 2048), desc_mnmajor(st + 16384 + kk * 2048), idesc,
+                     (first && kk == 0) ? 0u : 1u);
+    }
+    __device__ static void epi_begin(const Params&, const Sched&, int, int, Epi&) {}
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int v = (unit / sc.n_nt) * kBM + row;
+        const int n0 = (unit % sc.n_nt) * kBN;
+        const bool valid = v < p.V;
+        const bool first_chunk = p.chunk == 0;
+        float* out = p.dW + static_cast<int64_t>(valid ? v : 0) * p.d;
+        bool bad = false;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float x[32];
+            tmem_ld32(tacc + c * 32, x);
+            if (valid) {
+                float4* o4 = reinterpret_cast<float4*>(out + col0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float4 r = make_float4(x[4 * j] * sc.winv, x[4 * j + 1] * sc.winv, x[4 * j + 2] * sc.winv,
+                                           x[4 * j + 3] * sc.winv);
+                    if (!first_chunk) {
+                        const float4 o = o4[j];
+                        r.x += o.x;
+                        r.y += o.y;
+                        r.z += o.z;
+                        r.w += o.w;
+                    }
+                    bad |= !(isfinite(r.x) && isfinite(r.y) && isfinite(r.z) && isfinite(r.w));
+                    o4[j] = r;
+                }
+            }
+        }
+        if (bad) atomicOr(p.found_inf, 1);
+    }
+    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
+};
+
+// ====================================================================== engine
+
+template <class T, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ typename T::Params p, const __grid_constant__ CUtensorMap mA,
+              const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB) {
+    extern __shared__ uint8_t smem_raw[];
+    typename T::Sched sc;
+    if (!T::setup(p, sc)) return;
+    if (static_cast<int>(blockIdx.x) >= sc.n_units) return;   // no work: leave before touching TMEM
+
+    Smem sm = carve_smem<T::kStages, T::kStageBytes>(smem_raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int* status = p.status;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.acc_full[b], 1);
+            mbar_init(&sm.acc_empty[b], 4);
+        }
+        mbar_init(sm.drain, 1);
+        *sm.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&mA);
+        tma_prefetch_desc(&mA2);
+        tma_prefetch_desc(&mB);
+    }
+    if (warp == 1) {
+        tmem_alloc(sm.tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int unit = blockIdx.x; unit < sc.n_units; unit += gridDim.x) {
+                const int n_items = T::items(p, sc, unit);
+                const int ks = T::ksteps(p, sc, unit);
+                for (int item = 0; item < n_items; ++item) {
+                    const typename T::Coord c = T::coord(p, sc, unit, item);
+                    const uint32_t bytes = T::tx_bytes(p, c);
+                    for (int k = 0; k < ks; ++k) {
+                        if (!mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, status)) goto producer_done;
+                        uint8_t* st = sm.stages + s * T::kStageBytes;
+                        // post the expected byte count, then issue the copies that complete it
+                        mbar_arrive_expect_tx(&sm.full[s], bytes);
+                        T::load(p, c, k, st, &sm.full[s], &mA, &mA2, &mB);
+                        if (++s == T::kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int unit = blockIdx.x; unit < sc.n_units; unit += gridDim.x) {
+                const int n_items = T::items(p, sc, unit);
+                const int ks = T::ksteps(p, sc, unit);
+                for (int item = 0; item < n_items; ++item, ++it) {
+                    const int b = T::kAccBufs == 1 ? 0 : (it & 1);
+                    const uint32_t aph = static_cast<uint32_t>(T::kAccBufs == 1 ? it : (it >> 1)) & 1u;
+                    if (!mbar_wait(&sm.acc_empty[b], aph ^ 1u, sm.abort_flag, status)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t acc = tmem + b * T::kAccStride;
+                    for (int k = 0; k < ks; ++k) {
+                        if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, status)) goto mma_done;
+                        tc_fence_after();
+                        T::template mma<kBf16>(smem_u32(sm.stages + s * T::kStageBytes), acc, k == 0);
+                        umma_commit(&sm.empty[s]);
+                        if (++s == T::kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    umma_commit(&sm.acc_full[b]);
+                }
+            }
+        mma_done:
+            // every issued MMA must have finished before TMEM is released
+            umma_commit(sm.drain);
+            {
+                const uint32_t a = smem_u32(sm.drain);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(a, 0)) {
+                    if (globaltimer() - t0 > kWaitTimeoutNs) {
+                        atomicCAS(status, 0, GRPO_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue
+        const int row = lane + 32 * (warp & 3);
+        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        int it = 0;
+        for (int unit = blockIdx.x; unit < sc.n_units; unit += gridDim.x) {
+            const int n_items = T::items(p, sc, unit);
+            typename T::Epi e;
+            T::epi_begin(p, sc, unit, row, e);
+            for (int item = 0; item < n_items; ++item, ++it) {
+                const int b = T::kAccBufs == 1 ? 0 : (it & 1);
+                const uint32_t aph = static_cast<uint32_t>(T::kAccBufs == 1 ? it : (it >> 1)) & 1u;
+                if (!mbar_wait(&sm.acc_full[b], aph, sm.abort_flag, status)) goto epi_done;
+                tc_fence_after();
+                T::template epi_item<kBf16>(p, sc, unit, item, tq + b * T::kAccStride, e);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
+            }
+            T::epi_end(p, sc, unit, e);
+        }
+    epi_done:;
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ====================================================================== launches
+
+template <class T, bool kBf16>
+static cudaError_t launch_tc(const typename T::Params& p, const CUtensorMap& a, const CUtensorMap& a2,
+                             const CUtensorMap& b, int n_sm, cudaStream_t st) {
+    constexpr int smem = smem_bytes<T>();
+    auto kern = tc_kernel<T, kBf16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<n_sm, kThreads, smem, st>>>(p, a, a2, b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr, const CUtensorMap& mW,
+                       int n_sm, bool bf16, cudaStream_t st) {
+    return bf16 ? launch_tc<FwdT, true>(p, mHp, mHr, mW, n_sm, st) : launch_tc<FwdT, false>(p, mHp, mHr, mW, n_sm, st);
+}
+
+cudaError_t launch_ds(const ChunkParams& p, const CUtensorMap& mHc, const CUtensorMap& mW, int n_sm, bool bf16,
+                      cudaStream_t st) {
+    return bf16 ? launch_tc<DsT, true>(p, mHc, mHc, mW, n_sm, st) : launch_tc<DsT, false>(p, mHc, mHc, mW, n_sm, st);
+}
+
+cudaError_t launch_dh(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm, bool bf16,
+                      cudaStream_t st) {
+    return bf16 ? launch_tc<DhT, true>(p, mDS, mDS, mWmn, n_sm, st) : launch_tc<DhT, false>(p, mDS, mDS, mWmn, n_sm, st);
+}
+
+cudaError_t launch_dw(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm, bool bf16,
+                      cudaStream_t st) {
+    return bf16 ? launch_tc<DwT, true>(p, mDSmn, mDSmn, mHcmn, n_sm, st)
+                : launch_tc<DwT, false>(p, mDSmn, mDSmn, mHcmn, n_sm, st);
+}
+
+}  // namespace grpo
