@@ -1,0 +1,468 @@
+#!/usr/bin/env python
+"""Benchmark: fused linear GRPO loss forward+backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step = the whole hot path on one batch: group advantages, completion
+mask, row index, policy+reference lm_head logits with streaming logsumexp,
+objective and masked mean, and the recompute backward to dH and dW.  The
+default workload is the Llama-3.1-8B head at 20K context with 8 completions
+(G=8, L=20000, d=4096, V=128256, bf16), synthetic seeded inputs shaped like
+the pages' long-context run.  Inputs (W 1 GB, hidden states 1.3 GB each) are
+larger than L2, so steps need no L2 flush.
+
+Prints one JSON line (rank 0).  With N>1 (torchrun) each rank runs an
+independent replica of the same workload (the loss has no exchange on one
+GPU); value = all ranks' tokens / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of rows of the same workload, each step a different sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GRPO loss fwd+bwd tokens/s and % of bf16 tensor peak on 1 GB300; peak extra HBM"
+DEFAULT_CONFIG = "llama-3.1-8b-20k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--chunk-rows", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of one oracle sample")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- ranks
+
+class Ranks:
+    def __init__(self, n_gpus):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons every 200 ms."""
+
+    def __init__(self, gpu_uuid=None):
+        self.proc = None
+        self.path = None
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="grpo_clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+            if gpu_uuid:
+                cmd += ["-i", gpu_uuid]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons = [], [], set()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(REASON_NAMES, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_uuid():
+    try:
+        import torch
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------- helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("tc_kernels.cu", "ptx.cuh", "internal.h"):
+        h.update(open(os.path.join(ROOT, "rl_fine_tuning_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kind, config_name):
+    """DRAM bytes per launch of `kind` from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    ent = d.get("kernels", {}).get(kind)
+    if not ent:
+        return None
+    return ent.get("dram_bytes_per_launch_full_workload")
+
+
+def cfg_dict(cfg, extra=None):
+    d = {"workload": cfg.name, "G": cfg.G, "L": cfg.L, "N": cfg.N, "d": cfg.d, "V": cfg.V,
+         "global_batch": cfg.N, "seq_len": cfg.L, "beta": cfg.beta, "lengths": [cfg.len_lo, cfg.len_hi],
+         "parallelism": "replicas", "l2": "inputs larger than L2 (no flush)"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+def sample_rows(valid_rows, n, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    n = min(n, valid_rows.size)
+    return np.sort(rng.choice(valid_rows, size=n, replace=False)).astype(np.int32)
+
+
+def oracle_sample(cfg, wl, rows, adv):
+    """One bounded oracle run: per-row terms, dH and the dW contribution of the sampled rows."""
+    import oracle
+    t0 = time.perf_counter()
+    terms = oracle.row_terms(wl.h_pol, wl.h_ref, wl.W, cfg.dtype, wl.tokens, adv, cfg.L, rows, cfg.beta)
+    oracle.grad(wl.h_pol, wl.W, cfg.dtype, wl.tokens, rows, terms["lse_pol"], terms["g"], 1.0 / rows.size)
+    return time.perf_counter() - t0
+
+
+def oracle_rows_for(cfg, seconds, per_row_s=None):
+    # about 6*V*d fp64 multiply-adds per row; assume ~0.5 GMAC/s per host thread until measured
+    import oracle
+    thr = max(1, oracle.max_threads())
+    if per_row_s is None:
+        per_row_s = 6.0 * cfg.V * cfg.d / (0.5e9 * thr)
+    return max(thr, int(seconds / per_row_s))
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, ranks):
+    import numpy as np
+
+    import oracle
+    import synth
+    cfg = synth.make_config(args.config)
+    if ranks.rank != 0:
+        return
+    oracle.build()
+    synth.build()
+    wl = synth.generate(cfg, seed=0)
+    adv = oracle.group_advantages(wl.rewards, cfg.n_groups, cfg.G, cfg.eps, True)
+    mask = oracle.build_mask(wl.lengths, cfg.L)
+    valid = oracle.valid_rows(mask)
+    budget = max(2.0, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    # calibrate on a small sample, then size each step to the budget
+    cal = sample_rows(valid, max(1, oracle.max_threads()), 12345)
+    t_cal = oracle_sample(cfg, wl, cal, adv)
+    n_rows = max(1, int(budget / (t_cal / cal.size)))
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = sample_rows(valid, n_rows, 1000 + i)
+        dt = oracle_sample(cfg, wl, rows, adv)
+        if i >= args.warmup:
+            times.append((rows.size, dt))
+    toks = sum(n for n, _ in times)
+    secs = sum(t for _, t in times)
+    value = toks / secs
+    cores = oracle.max_threads()
+    sample = (f"{n_rows} seeded valid rows per step of {cfg.name} (of {valid.size}); per-row lse, q, p, KL, "
+              f"dH and dW contribution in fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": cfg_dict(cfg, {"sample_rows_per_step": n_rows}),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, ranks):
+    import numpy as np
+    import torch
+
+    import rl_fine_tuning_gb300 as rg
+    import synth
+
+    torch.cuda.set_device(ranks.local)
+    rg.load(build_if_missing=True)
+    cfg = synth.make_config(args.config)
+    wl = synth.generate(cfg, seed=0)
+    lengths_np = wl.lengths
+    n_valid = int(np.minimum(np.maximum(lengths_np, 0), cfg.L).sum())
+
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float16
+    shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.BF16 if cfg.dtype == "bf16" else rg.FP16,
+                          beta=cfg.beta, eps=cfg.eps, chunk_rows=args.chunk_rows)
+
+    def pinned(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory()
+
+    host = {"h_pol": pinned(wl.h_pol), "h_ref": pinned(wl.h_ref), "tokens": pinned(wl.tokens),
+            "lengths": pinned(wl.lengths), "rewards": pinned(wl.rewards)}
+    dev = {k: v.cuda() for k, v in host.items()}
+    dev["h_pol"] = dev["h_pol"].view(tdt)
+    dev["h_ref"] = dev["h_ref"].view(tdt)
+    W = torch.from_numpy(wl.W.view(np.int16)).cuda().view(tdt)
+    N, d, V = cfg.N, cfg.d, cfg.V
+    adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
+    mask = torch.empty(N, dtype=torch.uint8, device="cuda")
+    dH = torch.empty((N, d), dtype=tdt, device="cuda")
+    dW = torch.empty((V, d), dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    found_inf = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mem_before_ws = torch.cuda.memory_allocated()
+    ws_bytes = rg.grpo_workspace_bytes(shape)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    scale = [cfg.loss_scale]
+
+    def step(d_in):
+        rg.grpo_group_advantages(d_in["rewards"], cfg.n_groups, cfg.G, cfg.eps, True, adv)
+        rg.grpo_build_mask(d_in["lengths"], shape, mask)
+        rg.grpo_loss_fwd_bwd(d_in["h_pol"], d_in["h_ref"], W, d_in["tokens"], mask, adv, shape, scale[0], ws, loss,
+                             dH, dW, found_inf, None, status)
+
+    # warm-up (also settles the fp16 loss scale: halve while the scaled gradients overflow)
+    for _ in range(max(args.warmup, 1)):
+        step(dev)
+    torch.cuda.synchronize()
+    while cfg.dtype == "fp16" and int(found_inf.item()) == 1 and scale[0] > 1.0:
+        scale[0] /= 2
+        step(dev)
+        torch.cuda.synchronize()
+    st_code = int(status.item())
+    if st_code != 0:
+        raise SystemExit(f"device status {st_code}: {rg.grpo_status_string(st_code)}")
+    if not np.isfinite(loss.item()):
+        raise SystemExit("non-finite loss")
+
+    # ---------------- device-resident timed region
+    torch.cuda.reset_peak_memory_stats()
+    mem_base = torch.cuda.memory_allocated()
+    ranks.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_uuid())
+    rg.grpo_profile_enable(True)
+    launches0 = rg.grpo_kernel_launches()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(dev)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    rg.grpo_profile_enable(False)
+    launches = rg.grpo_kernel_launches() - launches0
+    prof = rg.grpo_profile_collect()
+    clocks = sampler.stop()
+    ranks.barrier()
+    ms = e0.elapsed_time(e1)
+    ms_max = ranks.max(ms)
+    peak_extra = torch.cuda.max_memory_allocated() - mem_base
+    ms_step = ms_max / args.steps
+    value = ranks.world * n_valid * args.steps / (ms_max / 1e3)
+
+    # ---------------- end to end: host inputs copied in, loss read back, every step
+    e2e = None
+    if not args.no_e2e:
+        loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
+        h2d = sum(host[k].numel() * host[k].element_size() for k in host)
+        d2h = 4
+
+        def e2e_step():
+            for k in host:
+                dev_raw = dev[k].view(host[k].dtype) if k in ("h_pol", "h_ref") else dev[k]
+                dev_raw.copy_(host[k], non_blocking=True)
+            step(dev)
+            loss_host.copy_(loss, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        ranks.barrier()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = ranks.max(a0.elapsed_time(a1))
+        e2e = {"value": ranks.world * n_valid * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps,
+               "resident": "lm_head weight W"}
+
+    # ---------------- roofline of the dominant kernel
+    pk, pk_kind = peaks()
+    flops_kind = {"fwd": 4.0 * n_valid * V * d, "ds": 2.0 * n_valid * V * d, "dh": 2.0 * n_valid * V * d,
+                  "dw": 2.0 * n_valid * V * d}
+    total_kernel_ms = sum(v[0] for v in prof.values())
+    kernels = {}
+    for k, (kms, cnt) in prof.items():
+        if cnt == 0:
+            continue
+        ent = {"ms_per_step": kms / args.steps, "launches_per_step": cnt / args.steps,
+               "share": kms / total_kernel_ms if total_kernel_ms > 0 else None}
+        if k in flops_kind and kms > 0:
+            ent["tflops"] = flops_kind[k] * args.steps / (kms / 1e3) / 1e12
+        kernels[k] = ent
+    dom = max(flops_kind, key=lambda k: prof[k][0])
+    dom_ms, dom_n = prof[dom]
+    sustained = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    achieved = flops_kind[dom] * args.steps / (dom_ms / 1e3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
+                "frac": achieved / sustained, "peak_kind": f"bf16 dense sustained, {pk_kind}",
+                "traffic": ncu_traffic(dom, cfg.name),
+                "flops_per_launch": flops_kind[dom] * args.steps / dom_n, "ms_per_launch": dom_ms / dom_n}
+    useful = 8.0 * n_valid * V * d
+    t_step = ms_step / 1e3
+    burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+
+    cpu = None
+    if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(cfg, wl, args)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ranks.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generator; random-init head)",
+        "config": cfg_dict(cfg, {"n_valid": n_valid, "chunk_rows": args.chunk_rows or 8192,
+                                 "loss_scale": scale[0]}),
+        "pct_bf16_peak": {"useful_tflops": useful / t_step / 1e12,
+                          "of_burst": useful / t_step / 1e12 / burst,
+                          "of_sustained": useful / t_step / 1e12 / sustained,
+                          "executed_tflops": 10.0 * n_valid * V * d / t_step / 1e12,
+                          "peaks": pk_kind},
+        "peak_extra_hbm_gb": max(peak_extra, 0) / 1e9 + ws_bytes / 1e9,
+        "workspace_gb": ws_bytes / 1e9,
+        "logits_not_materialised_gb": 2 * 2 * N * V / 1e9,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "kernels": kernels,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "loss": float(loss.item()),
+    }
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(cfg, wl, args):
+    """The oracle, as it stands, on the host cores: a bounded sample of rows."""
+    import oracle
+    oracle.build()
+    adv = oracle.group_advantages(wl.rewards, cfg.n_groups, cfg.G, cfg.eps, True)
+    valid = oracle.valid_rows(oracle.build_mask(wl.lengths, cfg.L))
+    cal = sample_rows(valid, max(1, oracle.max_threads()), 12345)
+    t_cal = oracle_sample(cfg, wl, cal, adv)
+    n = max(1, int(args.cpu_seconds / (t_cal / cal.size)))
+    rows = sample_rows(valid, n, 777)
+    dt = oracle_sample(cfg, wl, rows, adv)
+    return {"value": rows.size / dt, "unit": "tokens/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{rows.size} seeded valid rows of {cfg.name}: per-row lse/q/p/KL, dH and dW "
+                      f"contribution in fp64 ({dt:.1f} s)"}
+
+
+def main():
+    args = parse()
+    ranks = Ranks(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, ranks)
+        else:
+            run_ours(args, ranks)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -147,6 +147,32 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
                       void* dH, float* dW, int32_t* found_inf, float* row_stats,
                       int32_t* status, grpo_stream_t stream);
 
+/* ---- diagnostics ------------------------------------------------------
+ * Per-kernel device time.  While enabled, the library records a CUDA event
+ * pair on the launching stream around every kernel it launches.
+ * grpo_profile_collect waits for the recorded events, adds the elapsed
+ * milliseconds of each kernel kind into ms[kind] and the launch count into
+ * launches[kind] (arrays of at least GRPO_PROF_KINDS entries, caller-owned
+ * host memory), and clears the records.  Not thread-safe; meant for
+ * benchmarks.  grpo_kernel_launches counts every kernel launched by the
+ * library since it was loaded, profiling on or off. */
+enum {
+    GRPO_PROF_ADVANTAGES = 0,
+    GRPO_PROF_MASK,
+    GRPO_PROF_INDEX,
+    GRPO_PROF_FWD,
+    GRPO_PROF_MERGE,
+    GRPO_PROF_CLEAR,
+    GRPO_PROF_GATHER,
+    GRPO_PROF_DS,
+    GRPO_PROF_DH,
+    GRPO_PROF_DW,
+    GRPO_PROF_KINDS
+};
+int grpo_profile_enable(int on);
+int grpo_profile_collect(double* ms, long long* launches, int n_kinds);
+unsigned long long grpo_kernel_launches(void);
+
 /* Human-readable name of a status code (static string). */
 const char* grpo_status_string(int status);
 

@@ -17,8 +17,12 @@ from . import build as _build
 __all__ = [
     "GrpoError", "GrpoShape", "BF16", "FP16", "load", "make_shape", "grpo_workspace_bytes",
     "grpo_group_advantages", "grpo_build_mask", "grpo_valid_rows", "grpo_loss_fwd", "grpo_loss_fwd_bwd",
-    "grpo_status_string", "grpo_version", "library_path",
+    "grpo_status_string", "grpo_version", "library_path", "grpo_profile_enable", "grpo_profile_collect",
+    "grpo_kernel_launches", "PROF_KINDS",
 ]
+
+# kernel kinds of the diagnostics interface, in the order of the GRPO_PROF_* enum
+PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "ds", "dh", "dw")
 
 BF16, FP16 = 0, 1
 
@@ -74,6 +78,12 @@ def load(build_if_missing: bool = False):
     lib.grpo_status_string.argtypes = [i32]
     lib.grpo_status_string.restype = ctypes.c_char_p
     lib.grpo_version.restype = i32
+    lib.grpo_profile_enable.argtypes = [i32]
+    lib.grpo_profile_enable.restype = i32
+    lib.grpo_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), i32]
+    lib.grpo_profile_collect.restype = i32
+    lib.grpo_kernel_launches.argtypes = []
+    lib.grpo_kernel_launches.restype = ctypes.c_ulonglong
     for name in ("grpo_group_advantages", "grpo_build_mask", "grpo_valid_rows", "grpo_loss_fwd",
                  "grpo_loss_fwd_bwd"):
         getattr(lib, name).restype = i32
@@ -161,3 +171,20 @@ def grpo_status_string(code: int) -> str:
 
 def grpo_version() -> int:
     return int(load().grpo_version())
+
+
+def grpo_profile_enable(on: bool = True):
+    _check(load().grpo_profile_enable(int(bool(on))), "grpo_profile_enable")
+
+
+def grpo_profile_collect() -> dict:
+    """{kind: (milliseconds, launches)} accumulated since the last collect."""
+    n = len(PROF_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_longlong * n)()
+    _check(load().grpo_profile_collect(ms, cnt, n), "grpo_profile_collect")
+    return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(PROF_KINDS)}
+
+
+def grpo_kernel_launches() -> int:
+    return int(load().grpo_kernel_launches())

@@ -5,6 +5,9 @@
 #include <cstring>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <vector>
+
 #include "internal.h"
 
 namespace grpo {
@@ -12,6 +15,49 @@ namespace grpo {
 namespace {
 
 constexpr int kVersion = 100;   // 0.1.0
+
+// ---- launch accounting and optional per-kernel event timing
+std::atomic<unsigned long long> g_launches{0};
+
+struct ProfRecord {
+    int kind;
+    cudaEvent_t a, b;
+};
+
+struct Profiler {
+    bool on = false;
+    std::vector<ProfRecord> recs;
+    std::vector<cudaEvent_t> pool;
+    cudaEvent_t get() {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        return e;
+    }
+};
+Profiler g_prof;
+
+// launch one kernel through `fn`, counting it and timing it when profiling is on
+template <class F>
+cudaError_t launch(int kind, cudaStream_t st, F&& fn) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (g_prof.on) {
+        a = g_prof.get();
+        b = g_prof.get();
+        if (a) cudaEventRecord(a, st);
+    }
+    cudaError_t e = fn();
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (g_prof.on && a && b) {
+        cudaEventRecord(b, st);
+        g_prof.recs.push_back(ProfRecord{kind, a, b});
+    }
+    return e;
+}
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -165,8 +211,10 @@ int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     char* w = static_cast<char*>(in.ws);
     int* counts = reinterpret_cast<int*>(w + L.counts);
     cudaError_t e;
-    e = launch_index(in.mask, L.N, L.R, counts, reinterpret_cast<int*>(w + L.rows), reinterpret_cast<int2*>(w + L.tiles),
-                     in.status, nullptr, st);
+    e = launch(GRPO_PROF_INDEX, st, [&] {
+        return launch_index(in.mask, L.N, L.R, counts, reinterpret_cast<int*>(w + L.rows),
+                            reinterpret_cast<int2*>(w + L.tiles), in.status, nullptr, st);
+    });
     if (e != cudaSuccess) return GRPO_ERR_LAUNCH;
 
     CUtensorMap mHp, mHr, mW;
@@ -186,9 +234,13 @@ int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     fp.nps = L.nps;
     fp.n_ntiles = L.n_ntiles;
     fp.status = in.status;
-    if (launch_fwd(fp, mHp, mHr, mW, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
-    if (launch_merge(L, w, in.mask, in.tokens, in.adv, s.L, s.V, s.beta, in.loss_out, in.row_stats, in.status, st) !=
+    if (launch(GRPO_PROF_FWD, st, [&] { return launch_fwd(fp, mHp, mHr, mW, dev.sm_count, bf16, st); }) !=
         cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (launch(GRPO_PROF_MERGE, st, [&] {
+            return launch_merge(L, w, in.mask, in.tokens, in.adv, s.L, s.V, s.beta, in.loss_out, in.row_stats,
+                                in.status, st);
+        }) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
     return GRPO_OK;
 }
@@ -223,7 +275,9 @@ int grpo_group_advantages(const float* rewards, int n_groups, int G, float eps, 
                           grpo_stream_t stream) {
     if (n_groups < 1 || G < 1) return GRPO_ERR_SHAPE;
     if (!rewards || !adv_out || !aligned(rewards, 4) || !aligned(adv_out, 4)) return GRPO_ERR_POINTER;
-    return launch_advantages(rewards, n_groups, G, eps, std_unbiased, adv_out, reinterpret_cast<cudaStream_t>(stream)) ==
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return launch(GRPO_PROF_ADVANTAGES, st,
+                  [&] { return launch_advantages(rewards, n_groups, G, eps, std_unbiased, adv_out, st); }) ==
                    cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_LAUNCH;
@@ -232,8 +286,10 @@ int grpo_group_advantages(const float* rewards, int n_groups, int G, float eps, 
 int grpo_build_mask(const int32_t* lengths, const grpo_shape* shape, uint8_t* mask_out, grpo_stream_t stream) {
     if (!shape || !shape_ok(*shape)) return GRPO_ERR_SHAPE;
     if (!lengths || !mask_out || !aligned(lengths, 4)) return GRPO_ERR_POINTER;
-    return launch_build_mask(lengths, shape->n_groups * shape->G, shape->L, mask_out,
-                             reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return launch(GRPO_PROF_MASK, st,
+                  [&] { return launch_build_mask(lengths, shape->n_groups * shape->G, shape->L, mask_out, st); }) ==
+                   cudaSuccess
                ? GRPO_OK
                : GRPO_ERR_LAUNCH;
 }
@@ -250,8 +306,10 @@ int grpo_valid_rows(const uint8_t* mask, const grpo_shape* shape, int32_t* rows_
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     int* counts = reinterpret_cast<int*>(w + L.counts);
     int* scratch_status = counts + 8;
-    if (launch_index(mask, L.N, L.R, counts, rows_out, reinterpret_cast<int2*>(w + L.tiles), scratch_status, nullptr,
-                     st) != cudaSuccess)
+    if (launch(GRPO_PROF_INDEX, st, [&] {
+            return launch_index(mask, L.N, L.R, counts, rows_out, reinterpret_cast<int2*>(w + L.tiles),
+                                scratch_status, nullptr, st);
+        }) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
     if (cudaMemcpyAsync(n_valid_out, counts + C_NVALID, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
@@ -295,9 +353,12 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     if (rc != GRPO_OK) return rc;
 
     // zero the reported overflow flag and the masked rows of dH; dW when nothing is masked in
-    if (launch_clear_grads(counts, found_inf, dW, static_cast<int64_t>(s.V) * s.d, st) != cudaSuccess)
+    if (launch(GRPO_PROF_CLEAR, st,
+               [&] { return launch_clear_grads(counts, found_inf, dW, static_cast<int64_t>(s.V) * s.d, st); }) !=
+        cudaSuccess)
         return GRPO_ERR_LAUNCH;
-    if (launch_zero_masked_rows(mask, L.N, s.d, dH, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    if (launch(GRPO_PROF_CLEAR, st, [&] { return launch_zero_masked_rows(mask, L.N, s.d, dH, st); }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
 
     CUtensorMap mW_k, mW_mn, mHc_k, mHc_mn, mDS_k, mDS_mn;
     void* hc = w + L.hc;
@@ -326,10 +387,17 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     const int64_t max_chunks = (L.N + L.R - 1) / L.R;
     for (int64_t c = 0; c < max_chunks; ++c) {
         cp.chunk = static_cast<int>(c);
-        if (launch_gather_rows(cp, h_pol, hc, L.R, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
-        if (launch_ds(cp, mHc_k, mW_k, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
-        if (launch_dh(cp, mDS_k, mW_mn, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
-        if (launch_dw(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st) != cudaSuccess) return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_GATHER, st, [&] { return launch_gather_rows(cp, h_pol, hc, L.R, st); }) != cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_DS, st, [&] { return launch_ds(cp, mHc_k, mW_k, dev.sm_count, bf16, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_DH, st, [&] { return launch_dh(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_DW, st, [&] { return launch_dw(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
     }
     return GRPO_OK;
 }
@@ -349,5 +417,30 @@ const char* grpo_status_string(int status) {
 }
 
 int grpo_version(void) { return kVersion; }
+
+int grpo_profile_enable(int on) {
+    g_prof.on = on != 0;
+    return GRPO_OK;
+}
+
+int grpo_profile_collect(double* ms, long long* launches, int n_kinds) {
+    if ((!ms || !launches) && n_kinds > 0) return GRPO_ERR_POINTER;
+    int rc = GRPO_OK;
+    for (const ProfRecord& r : g_prof.recs) {
+        float t = 0.f;
+        if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+            rc = GRPO_ERR_LAUNCH;
+        if (r.kind < n_kinds) {
+            ms[r.kind] += static_cast<double>(t);
+            launches[r.kind] += 1;
+        }
+        g_prof.pool.push_back(r.a);
+        g_prof.pool.push_back(r.b);
+    }
+    g_prof.recs.clear();
+    return rc;
+}
+
+unsigned long long grpo_kernel_launches(void) { return g_launches.load(); }
 
 }  // extern "C"
