@@ -147,6 +147,29 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
                       void* dH, float* dW, int32_t* found_inf, float* row_stats,
                       int32_t* status, grpo_stream_t stream);
 
+/* Forward loss for callers that cannot allocate device memory -- for
+ * instance a training step that shares the GPU with an inference engine
+ * which has already reserved all free memory for its own pool, or code that
+ * cannot afford cudaMalloc's device-wide synchronisation inside its step.
+ * The pages have no counterpart of this entry point; it is a property of
+ * this library, not of the method.
+ *
+ * Same inputs and outputs as grpo_loss_fwd, without the workspace: the
+ * library uses an 8 MiB array of its own, held on every GPU that loads the
+ * library until the process exits.  It allocates nothing and calls no
+ * allocating routine.
+ *   Limit: N = n_groups*G*L <= 32768 rows; larger shapes are rejected with
+ *   GRPO_ERR_WORKSPACE before anything is launched.
+ *   The first call on a device looks up the array's device address (a
+ *   synchronous runtime call); make that first call before any stream
+ *   capture.
+ *   Every call uses the same array, so calls that can overlap on the GPU
+ *   (other streams, other host threads) race; serialise them.  Nothing
+ *   carries over between calls: each call writes every word it reads. */
+int grpo_loss_fwd_noalloc(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                          const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                          float* loss_out, float* row_stats, int32_t* status, grpo_stream_t stream);
+
 /* ---- diagnostics ------------------------------------------------------
  * Per-kernel device time.  While enabled, the library records a CUDA event
  * pair on the launching stream around every kernel it launches.

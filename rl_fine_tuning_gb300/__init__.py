@@ -188,3 +188,14 @@ def grpo_profile_collect() -> dict:
 
 def grpo_kernel_launches() -> int:
     return int(load().grpo_kernel_launches())
+
+
+def grpo_loss_fwd_noalloc(h_pol, h_ref, W, tokens, mask, adv, shape, loss_out, row_stats, status, stream=None):
+    """grpo_loss_fwd on the library's own fixed scratch array (no workspace argument)."""
+    fn = load().grpo_loss_fwd_noalloc
+    if fn.argtypes is None:
+        p = ctypes.c_void_p
+        fn.argtypes = [p, p, p, p, p, p, ctypes.POINTER(GrpoShape), p, p, p, p]
+        fn.restype = ctypes.c_int
+    _check(fn(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv), ctypes.byref(shape),
+              _ptr(loss_out), _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_noalloc")

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <mutex>
 #include <vector>
 
 #include "internal.h"
@@ -444,3 +445,69 @@ int grpo_profile_collect(double* ms, long long* launches, int n_kinds) {
 unsigned long long grpo_kernel_launches(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward loss without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they need the loss: a
+// training step that runs next to an inference engine which has reserved all
+// free device memory for its own pool (the pages describe sharing one CUDA
+// memory space with vLLM), or code that must not pay for cudaMalloc's
+// device-wide synchronisation inside its step.  This entry point serves them
+// from a fixed array that lives in the library itself.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(8) << 20;   // 8 MiB on every device
+constexpr int64_t kNoAllocMaxRows = 32768;                                // n_groups * G * L
+constexpr int kNoAllocMaxDevices = 256;
+
+// The forward's workspace.  Every GPU that loads the library holds these
+// 8 MiB until the process exits.  In host code the name is only a handle:
+// kernels get the device address looked up below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+// Device address of the array on the current device, looked up once per device.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return GRPO_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GRPO_ERR_LAUNCH;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return GRPO_OK;
+}
+
+}  // namespace
+
+extern "C" int grpo_loss_fwd_noalloc(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                                     const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                                     float* loss_out, float* row_stats, int32_t* status, grpo_stream_t stream) {
+    if (!shape) return GRPO_ERR_SHAPE;
+    if (!dtype_ok(*shape)) return GRPO_ERR_DTYPE;
+    WsLayout L;
+    if (!ws_layout(*shape, &L)) return GRPO_ERR_SHAPE;
+    // the forward only touches the workspace below the backward buffers (L.hc)
+    if (L.N > kNoAllocMaxRows || L.hc > kNoAllocScratchBytes) return GRPO_ERR_WORKSPACE;
+    if (!h_pol || !h_ref || !W || !tokens || !mask || !adv || !loss_out || !status) return GRPO_ERR_POINTER;
+    if (!aligned(h_pol, 16) || !aligned(h_ref, 16) || !aligned(W, 16) || !aligned(tokens, 4) || !aligned(adv, 4) ||
+        !aligned(loss_out, 4) || !aligned(status, 4) || (row_stats && !aligned(row_stats, 4)))
+        return GRPO_ERR_POINTER;
+    DeviceInfo dev;
+    int rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != GRPO_OK) return rc;
+    // Nothing in the array needs clearing: every word the forward reads is
+    // written earlier in the same call (row index, per-split partials of the
+    // masked-in rows, per-block sums).
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, scratch, L.hc, loss_out, row_stats, status};
+    return run_forward(in, L, dev, reinterpret_cast<cudaStream_t>(stream));
+}
