@@ -1,0 +1,118 @@
+"""Host-side checks of libgrpo that need no GPU: the library loads, exports
+every function include/grpo.h declares, agrees with the binding on the shape
+struct, sizes its workspace, and rejects bad arguments before any launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "grpo.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rl_fine_tuning_gb300 import build
+    build.build()
+    import rl_fine_tuning_gb300 as rg
+    return rg.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(grpo_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (grpo_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_shape_struct_layout_matches_binding(tmp_path):
+    import rl_fine_tuning_gb300 as rg
+    prog = tmp_path / "sz.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "grpo.h"\n'
+                    'int main(void){printf("%zu", sizeof(grpo_shape));'
+                    'const char* n[]={"n_groups","G","L","d","V","dtype","beta","eps","std_unbiased","chunk_rows"};'
+                    'size_t o[]={offsetof(grpo_shape,n_groups),offsetof(grpo_shape,G),offsetof(grpo_shape,L),'
+                    'offsetof(grpo_shape,d),offsetof(grpo_shape,V),offsetof(grpo_shape,dtype),'
+                    'offsetof(grpo_shape,beta),offsetof(grpo_shape,eps),offsetof(grpo_shape,std_unbiased),'
+                    'offsetof(grpo_shape,chunk_rows)};'
+                    'for(int i=0;i<10;i++)printf(" %s=%zu",n[i],o[i]);return 0;}\n')
+    exe = tmp_path / "sz"
+    subprocess.check_call(["gcc", "-I" + os.path.join(ROOT, "include"), str(prog), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split()
+    assert int(out[0]) == ctypes.sizeof(rg.GrpoShape)
+    for item in out[1:]:
+        k, v = item.split("=")
+        assert getattr(rg.GrpoShape, k).offset == int(v), k
+
+
+def test_shape_defaults_and_workspace_bytes(lib):
+    import rl_fine_tuning_gb300 as rg
+    s = rg.make_shape(1, 8, 20000, 4096, 128256)
+    assert (s.beta, s.std_unbiased, s.chunk_rows) == (pytest.approx(0.04), 1, 0)
+    assert s.eps == pytest.approx(1e-4)
+    n = rg.grpo_workspace_bytes(s)
+    N, R, V, d = 160000, 8192, 128256, 4096
+    # O(R*V + R*d + N) -- never O(N*V)
+    assert R * V * 2 <= n < R * V * 2 + R * d * 2 + 300 * N + (1 << 20)
+    assert n < 2 * 2 * N * V // 30
+    s2 = rg.make_shape(1, 8, 20000, 4096, 128256, chunk_rows=4096)
+    assert rg.grpo_workspace_bytes(s2) < n
+    for bad in (dict(d=100), dict(d=0), dict(V=0), dict(G=0), dict(L=0)):
+        b = rg.make_shape(1, 8, 20000, 4096, 128256)
+        for k, v in bad.items():
+            setattr(b, k, v)
+        assert rg.grpo_workspace_bytes(b) == 0, bad
+
+
+def test_validation_codes_without_a_device(lib):
+    """Argument errors come back as status codes before anything touches a GPU."""
+    import rl_fine_tuning_gb300 as rg
+    s = rg.make_shape(1, 4, 64, 128, 1024)
+    need = rg.grpo_workspace_bytes(s)
+    P = 1 << 20                         # a 256-byte aligned stand-in address, never dereferenced
+    f = lib.grpo_loss_fwd
+    args = [P, P, P, P, P, P, ctypes.byref(s), P, need, P, None, P, None]
+    assert f(*args[:7], None, need, *args[9:]) == 1                      # null workspace
+    assert f(*args[:7], P + 8, need, *args[9:]) == 1                     # misaligned workspace
+    assert f(P + 2, *args[1:]) == 1                                      # misaligned h_pol
+    assert f(*args[:7], P, need - 1, *args[9:]) == 3                     # workspace too small
+    bad = rg.make_shape(1, 4, 64, 100, 1024)
+    assert f(*args[:6], ctypes.byref(bad), *args[7:]) == 2               # d not a multiple of 64
+    bad.dtype = 7
+    assert f(*args[:6], ctypes.byref(bad), *args[7:]) == 5               # unknown dtype
+    assert lib.grpo_group_advantages(P, 0, 4, ctypes.c_float(1e-4), 1, P, None) == 2
+    assert lib.grpo_group_advantages(None, 1, 4, ctypes.c_float(1e-4), 1, P, None) == 1
+    fb = lib.grpo_loss_fwd_bwd
+    assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(1.0), P, need, P, None, P, P, None, P, None) == 1
+    assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(0.0), P, need, P, P, P, P, None, P, None) == 2
+    assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(float("nan")), P, need, P, P, P, P, None, P,
+              None) == 2
+
+
+def test_status_strings_and_version(lib):
+    import rl_fine_tuning_gb300 as rg
+    assert rg.grpo_status_string(0) == "ok"
+    assert "workspace" in rg.grpo_status_string(3)
+    assert "timed out" in rg.grpo_status_string(6)
+    assert rg.grpo_version() >= 100
+    assert rg.grpo_kernel_launches() == 0 or rg.grpo_kernel_launches() > 0
+
+
+def test_binding_refuses_to_run_without_the_library(tmp_path, monkeypatch):
+    import rl_fine_tuning_gb300 as rg
+    from rl_fine_tuning_gb300 import build
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(rg, "_lib", None)
+    with pytest.raises(ImportError):
+        rg.load()
