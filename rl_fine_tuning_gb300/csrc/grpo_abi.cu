@@ -221,7 +221,7 @@ int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     CUtensorMap mHp, mHr, mW;
     if (!make_map(&mHp, in.h_pol, bf16, s.d, L.N, s.d, kBK, kBM) ||
         !make_map(&mHr, in.h_ref, bf16, s.d, L.N, s.d, kBK, kBM) ||
-        !make_map(&mW, in.W, bf16, s.d, s.V, s.d, kBK, kBN))
+        !make_map(&mW, in.W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterFwd))
         return GRPO_ERR_LAUNCH;
     FwdParams fp;
     fp.tiles = reinterpret_cast<const int2*>(w + L.tiles);
@@ -229,6 +229,7 @@ int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     fp.tokens = in.tokens;
     fp.part = reinterpret_cast<float4*>(w + L.part);
     fp.zt = reinterpret_cast<float2*>(w + L.zt);
+    fp.N = L.N;
     fp.V = s.V;
     fp.d = s.d;
     fp.S = L.S;
@@ -364,7 +365,8 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     CUtensorMap mW_k, mW_mn, mHc_k, mHc_mn, mDS_k, mDS_mn;
     void* hc = w + L.hc;
     void* ds = w + L.ds;
-    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN) || !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) ||
+    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterBwd) ||
+        !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) ||
         !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) || !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
         !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
         !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK))

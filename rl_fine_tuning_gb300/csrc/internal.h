@@ -16,6 +16,9 @@ constexpr int kMaxFwdSplits = 8;      // vocabulary splits of one forward row ti
 constexpr int kDefaultChunkRows = 8192;
 constexpr int kMergeThreads = 256;
 constexpr int kIndexThreads = 1024;
+// CTAs per cluster sharing one B tile through TMA multicast (1, 2 or 4)
+constexpr int kClusterFwd = 2;
+constexpr int kClusterBwd = 2;
 
 // int32 words at the start of the workspace
 enum CountSlot {
@@ -46,6 +49,7 @@ struct FwdParams {
     const int* tokens;
     float4* part;           // [N x S] (m_pol, s_pol, m_ref, s_ref)
     float2* zt;             // [N] (z_pol[tok], z_ref[tok])
+    int64_t N;
     int V, d, S, nps, n_ntiles;
     int* status;
 };
