@@ -139,8 +139,9 @@ int grpo_loss_fwd(const void* h_pol, const void* h_ref, const void* W, const int
  *   found_inf: one int32 (device) <- 1 if any scaled gradient value (the
  *               16-bit dlogits, dH or dW) is not finite, else 0.  The caller
  *               lowers the scale and calls again when it is set.
- * The loss equals grpo_loss_fwd's bit for bit; dH and dW are bitwise
- * reproducible (fixed reduction order, no floating-point atomics). */
+ * The loss matches grpo_loss_fwd's to fp32 rounding (the two split the
+ * vocabulary differently); every output is bitwise reproducible from run to
+ * run (fixed reduction orders, no floating-point atomics). */
 int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
                       const uint8_t* mask, const float* adv, const grpo_shape* shape,
                       float loss_scale, void* workspace, size_t ws_bytes, float* loss_out,

@@ -140,32 +140,47 @@ int chunk_rows_of(const grpo_shape& s) {
 
 }  // namespace
 
+// splits of n_ntiles vocabulary tiles into at most max_splits ranges, none empty
+static void split_vocab(int n_ntiles, int max_splits, int* S, int* nps) {
+    int s = n_ntiles < max_splits ? n_ntiles : max_splits;
+    *nps = (n_ntiles + s - 1) / s;
+    *S = (n_ntiles + *nps - 1) / *nps;
+}
+
 bool ws_layout(const grpo_shape& s, WsLayout* o) {
     if (!shape_ok(s)) return false;
     const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
     o->N = N;
     o->n_ntiles = (s.V + kBN - 1) / kBN;
-    int S = o->n_ntiles < kMaxFwdSplits ? o->n_ntiles : kMaxFwdSplits;
-    o->nps = (o->n_ntiles + S - 1) / S;
-    o->S = (o->n_ntiles + o->nps - 1) / o->nps;   // no empty split
+    split_vocab(o->n_ntiles, kTileSplits, &o->S, &o->nps);
+    split_vocab(o->n_ntiles, kChunkSplits, &o->Sc, &o->npsc);
     o->R = chunk_rows_of(s);
     o->V_pad = (s.V + 63) / 64 * 64;
+    o->nc32 = (s.V + 31) / 32;
     o->nblk = static_cast<int>((N + kMergeThreads - 1) / kMergeThreads);
+    o->n_sched = static_cast<int>(2 + (N + o->R - 1) / o->R);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
         off = align_up(off + bytes, 256);
         return at;
     };
+    // forward-only path (also what the workspace-free forward uses): everything below `hc`
     o->counts = take(C_COUNT_WORDS * 4);
+    o->sched = take(static_cast<size_t>(o->n_sched) * 4);
     o->tiles = take(static_cast<size_t>(N) * 8);
     o->rows = take(static_cast<size_t>(N) * 4);
     o->part = take(static_cast<size_t>(N) * o->S * 16);
     o->zt = take(static_cast<size_t>(N) * 8);
     o->lse = take(static_cast<size_t>(N) * 4);
     o->gco = take(static_cast<size_t>(N) * 4);
+    o->ell = take(static_cast<size_t>(N) * 4);
     o->blocksum = take(static_cast<size_t>(o->nblk) * 8);
+    // backward chunk buffers
     o->hc = take(static_cast<size_t>(o->R) * s.d * 2);
+    o->hcr = take(static_cast<size_t>(o->R) * s.d * 2);
+    o->partc = take(static_cast<size_t>(o->R) * o->Sc * 16);
+    o->mx = take(static_cast<size_t>(o->R) * o->nc32 * 4);
     o->ds = take(static_cast<size_t>(o->R) * o->V_pad * 2);
     o->total = off;
     return true;
@@ -206,45 +221,94 @@ int validate(const Inputs& in, WsLayout* L) {
     return GRPO_OK;
 }
 
+MergeParams merge_params(const Inputs& in, const WsLayout& L, char* w, int chunk, const float4* part, int S) {
+    const grpo_shape& s = *in.shape;
+    MergeParams mp;
+    mp.part = part;
+    mp.zt = reinterpret_cast<const float2*>(w + L.zt);
+    mp.mask = in.mask;
+    mp.tokens = in.tokens;
+    mp.adv = in.adv;
+    mp.counts = reinterpret_cast<const int*>(w + L.counts);
+    mp.rows = reinterpret_cast<const int*>(w + L.rows);
+    mp.chunk = chunk;
+    mp.R = L.R;
+    mp.S = S;
+    mp.L = s.L;
+    mp.V = s.V;
+    mp.beta = s.beta;
+    mp.N = L.N;
+    mp.lse = reinterpret_cast<float*>(w + L.lse);
+    mp.gco = reinterpret_cast<float*>(w + L.gco);
+    mp.ell = reinterpret_cast<float*>(w + L.ell);
+    mp.row_stats = in.row_stats;
+    mp.status = in.status;
+    return mp;
+}
+
+FwdParams fwd_params(const Inputs& in, const WsLayout& L, char* w) {
+    const grpo_shape& s = *in.shape;
+    FwdParams fp = {};
+    fp.counts = reinterpret_cast<const int*>(w + L.counts);
+    fp.rows = reinterpret_cast<const int*>(w + L.rows);
+    fp.tokens = in.tokens;
+    fp.zt = reinterpret_cast<float2*>(w + L.zt);
+    fp.N = L.N;
+    fp.V = s.V;
+    fp.d = s.d;
+    fp.n_ntiles = L.n_ntiles;
+    fp.V_pad = L.V_pad;
+    fp.nc32 = L.nc32;
+    fp.status = in.status;
+    return fp;
+}
+
+int run_index(const Inputs& in, const WsLayout& L, char* w, cudaStream_t st) {
+    return launch(GRPO_PROF_INDEX, st, [&] {
+               return launch_index(in.mask, L.N, L.R, reinterpret_cast<int*>(w + L.counts),
+                                   reinterpret_cast<int*>(w + L.rows), reinterpret_cast<int2*>(w + L.tiles),
+                                   reinterpret_cast<int*>(w + L.sched), L.n_sched, in.status, st);
+           }) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_LAUNCH;
+}
+
+int run_loss_reduce(const Inputs& in, const WsLayout& L, char* w, cudaStream_t st) {
+    return launch(GRPO_PROF_MERGE, st, [&] {
+               return launch_loss_reduce(reinterpret_cast<const float*>(w + L.ell), L.N,
+                                         reinterpret_cast<double*>(w + L.blocksum), L.nblk,
+                                         reinterpret_cast<const int*>(w + L.counts), in.loss_out, st);
+           }) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_LAUNCH;
+}
+
+// Forward over all rows at once: row tiles of h_pol / h_ref, per-row merge,
+// loss reduction.  Touches only the workspace below the chunk buffers.
 int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cudaStream_t st) {
     const grpo_shape& s = *in.shape;
     const bool bf16 = s.dtype == GRPO_BF16;
     char* w = static_cast<char*>(in.ws);
-    int* counts = reinterpret_cast<int*>(w + L.counts);
-    cudaError_t e;
-    e = launch(GRPO_PROF_INDEX, st, [&] {
-        return launch_index(in.mask, L.N, L.R, counts, reinterpret_cast<int*>(w + L.rows),
-                            reinterpret_cast<int2*>(w + L.tiles), in.status, nullptr, st);
-    });
-    if (e != cudaSuccess) return GRPO_ERR_LAUNCH;
-
+    int rc = run_index(in, L, w, st);
+    if (rc != GRPO_OK) return rc;
     CUtensorMap mHp, mHr, mW;
     if (!make_map(&mHp, in.h_pol, bf16, s.d, L.N, s.d, kBK, kBM) ||
         !make_map(&mHr, in.h_ref, bf16, s.d, L.N, s.d, kBK, kBM) ||
         !make_map(&mW, in.W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterFwd))
         return GRPO_ERR_LAUNCH;
-    FwdParams fp;
+    FwdParams fp = fwd_params(in, L, w);
     fp.tiles = reinterpret_cast<const int2*>(w + L.tiles);
-    fp.counts = counts;
-    fp.tokens = in.tokens;
     fp.part = reinterpret_cast<float4*>(w + L.part);
-    fp.zt = reinterpret_cast<float2*>(w + L.zt);
-    fp.N = L.N;
-    fp.V = s.V;
-    fp.d = s.d;
     fp.S = L.S;
     fp.nps = L.nps;
-    fp.n_ntiles = L.n_ntiles;
-    fp.status = in.status;
+    fp.sched = reinterpret_cast<int*>(w + L.sched);
+    fp.chunk = -1;
     if (launch(GRPO_PROF_FWD, st, [&] { return launch_fwd(fp, mHp, mHr, mW, dev.sm_count, bf16, st); }) !=
         cudaSuccess)
         return GRPO_ERR_LAUNCH;
-    if (launch(GRPO_PROF_MERGE, st, [&] {
-            return launch_merge(L, w, in.mask, in.tokens, in.adv, s.L, s.V, s.beta, in.loss_out, in.row_stats,
-                                in.status, st);
-        }) != cudaSuccess)
-        return GRPO_ERR_LAUNCH;
-    return GRPO_OK;
+    const MergeParams mp = merge_params(in, L, w, -1, reinterpret_cast<const float4*>(w + L.part), L.S);
+    if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    return run_loss_reduce(in, L, w, st);
 }
 
 }  // namespace
@@ -310,7 +374,7 @@ int grpo_valid_rows(const uint8_t* mask, const grpo_shape* shape, int32_t* rows_
     int* scratch_status = counts + 8;
     if (launch(GRPO_PROF_INDEX, st, [&] {
             return launch_index(mask, L.N, L.R, counts, rows_out, reinterpret_cast<int2*>(w + L.tiles),
-                                scratch_status, nullptr, st);
+                                reinterpret_cast<int*>(w + L.sched), L.n_sched, scratch_status, st);
         }) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
     if (cudaMemcpyAsync(n_valid_out, counts + C_NVALID, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
@@ -351,26 +415,39 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     char* w = static_cast<char*>(workspace);
     int* counts = reinterpret_cast<int*>(w + L.counts);
 
-    rc = run_forward(in, L, dev, st);
+    rc = run_index(in, L, w, st);
     if (rc != GRPO_OK) return rc;
-
-    // zero the reported overflow flag and the masked rows of dH; dW when nothing is masked in
+    // found_inf <- 0 (dW <- 0 when no row is masked in); masked rows: objective 0, dH rows 0
     if (launch(GRPO_PROF_CLEAR, st,
                [&] { return launch_clear_grads(counts, found_inf, dW, static_cast<int64_t>(s.V) * s.d, st); }) !=
         cudaSuccess)
         return GRPO_ERR_LAUNCH;
+    if (launch(GRPO_PROF_CLEAR, st, [&] {
+            return launch_rows_init(mask, L.N, reinterpret_cast<float*>(w + L.ell), row_stats, st);
+        }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
     if (launch(GRPO_PROF_CLEAR, st, [&] { return launch_zero_masked_rows(mask, L.N, s.d, dH, st); }) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
 
-    CUtensorMap mW_k, mW_mn, mHc_k, mHc_mn, mDS_k, mDS_mn;
+    CUtensorMap mW_k, mW_mn, mHc_k, mHcr_k, mHc_mn, mDS_k, mDS_mn;
     void* hc = w + L.hc;
+    void* hcr = w + L.hcr;
     void* ds = w + L.ds;
-    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterBwd) ||
-        !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) ||
-        !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) || !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
+    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterFwd) ||
+        !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) || !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
+        !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
+        !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
         !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
         !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK))
         return GRPO_ERR_LAUNCH;
+
+    FwdParams fp = fwd_params(in, L, w);
+    fp.tiles = nullptr;                                  // chunk mode
+    fp.part = reinterpret_cast<float4*>(w + L.partc);
+    fp.S = L.Sc;
+    fp.nps = L.npsc;
+    fp.E = static_cast<uint16_t*>(ds);
+    fp.mx = reinterpret_cast<float*>(w + L.mx);
 
     ChunkParams cp;
     cp.counts = counts;
@@ -378,22 +455,34 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     cp.tokens = tokens;
     cp.lse = reinterpret_cast<const float*>(w + L.lse);
     cp.gco = reinterpret_cast<const float*>(w + L.gco);
+    cp.zt = reinterpret_cast<const float2*>(w + L.zt);
+    cp.mx = reinterpret_cast<const float*>(w + L.mx);
     cp.scale = loss_scale;
     cp.V = s.V;
     cp.d = s.d;
     cp.V_pad = L.V_pad;
+    cp.nc32 = L.nc32;
     cp.dS = static_cast<uint16_t*>(ds);
     cp.dH = static_cast<uint16_t*>(dH);
     cp.dW = dW;
+    cp.sched = nullptr;
     cp.found_inf = found_inf;
     cp.status = status;
     const int64_t max_chunks = (L.N + L.R - 1) / L.R;
     for (int64_t c = 0; c < max_chunks; ++c) {
-        cp.chunk = static_cast<int>(c);
-        if (launch(GRPO_PROF_GATHER, st, [&] { return launch_gather_rows(cp, h_pol, hc, L.R, st); }) != cudaSuccess)
-            return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DS, st, [&] { return launch_ds(cp, mHc_k, mW_k, dev.sm_count, bf16, st); }) !=
+        const int ci = static_cast<int>(c);
+        cp.chunk = ci;
+        fp.chunk = ci;
+        fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
+        const MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
+        if (launch(GRPO_PROF_GATHER, st, [&] { return launch_gather_rows(cp, h_pol, hc, h_ref, hcr, L.R, st); }) !=
             cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_FWD, st, [&] { return launch_fwd(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_DS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_DH, st, [&] { return launch_dh(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
             cudaSuccess)
@@ -402,7 +491,7 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
     }
-    return GRPO_OK;
+    return run_loss_reduce(in, L, w, st);
 }
 
 const char* grpo_status_string(int status) {

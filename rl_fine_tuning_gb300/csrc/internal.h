@@ -12,12 +12,14 @@ namespace grpo {
 constexpr int kBM = 128;              // rows (or vocabulary rows for dW) per MMA tile
 constexpr int kBK = 64;               // K elements per pipeline stage: one 128-byte swizzle span
 constexpr int kBN = 256;              // accumulator columns per MMA tile
-constexpr int kMaxFwdSplits = 8;      // vocabulary splits of one forward row tile
+constexpr int kTileSplits = 8;        // vocabulary splits of a forward row tile (forward-only path)
+constexpr int kChunkSplits = 64;      // vocabulary splits of a chunk row tile (forward+backward path)
 constexpr int kDefaultChunkRows = 8192;
 constexpr int kMergeThreads = 256;
 constexpr int kIndexThreads = 1024;
+constexpr int kTransformThreads = 256;
 // CTAs per cluster sharing one B tile through TMA multicast (1, 2 or 4)
-constexpr int kClusterFwd = 2;
+constexpr int kClusterFwd = 1;
 constexpr int kClusterBwd = 2;
 
 // int32 words at the start of the workspace
@@ -31,26 +33,37 @@ enum CountSlot {
 };
 
 struct WsLayout {
-    size_t counts, tiles, rows, part, zt, lse, gco, blocksum, hc, ds, total;
-    int S;           // forward vocabulary splits
-    int nps;         // vocabulary N-tiles per split
+    size_t counts, sched, tiles, rows, part, zt, lse, gco, ell, blocksum, hc, hcr, partc, mx, ds, total;
+    int S, nps;      // forward-only path: vocabulary splits, N-tiles per split (partials by row)
+    int Sc, npsc;    // chunked path: vocabulary splits, N-tiles per split (partials by chunk slot)
     int n_ntiles;    // ceil(V / kBN)
     int R;           // rows per backward chunk (buffer height)
     int V_pad;       // row pitch of the dlogits buffer, elements
-    int nblk;        // merge blocks
+    int nc32;        // 32-column groups per vocabulary row
+    int nblk;        // loss-reduction blocks
+    int n_sched;     // scheduler counters
     int64_t N;
 };
 
 bool ws_layout(const grpo_shape& s, WsLayout* out);
 
+// Forward logits + streaming logsumexp.  Two row sources:
+//   tiles != nullptr : forward row tiles over h_pol / h_ref (runs of masked-in rows)
+//   tiles == nullptr : the compact rows of backward chunk `chunk` (gathered copies);
+//                      then E/mx receive exp(z_pol - running max) and the running max
 struct FwdParams {
-    const int2* tiles;      // (first row, rows) per forward tile
+    const int2* tiles;      // (first row, rows) per forward tile, or nullptr
     const int* counts;
+    const int* rows;        // valid-row list (chunk mode)
     const int* tokens;
-    float4* part;           // [N x S] (m_pol, s_pol, m_ref, s_ref)
+    float4* part;           // (m_pol, s_pol, m_ref, s_ref): [N x S] by row, or [R x S] by chunk slot
     float2* zt;             // [N] (z_pol[tok], z_ref[tok])
+    uint16_t* E;            // [R x V_pad] bf16 exp(z_pol - m) (chunk mode, may be nullptr)
+    float* mx;              // [R x nc32] running max after each 32-column group (chunk mode)
+    int* sched;             // zeroed work counter of this launch
     int64_t N;
-    int V, d, S, nps, n_ntiles;
+    int chunk;
+    int V, d, S, nps, n_ntiles, V_pad, nc32;
     int* status;
 };
 
@@ -60,26 +73,52 @@ struct ChunkParams {
     const int* tokens;
     const float* lse;       // [N] policy logsumexp
     const float* gco;       // [N] d ell / d q
+    const float2* zt;       // [N] (z_pol[tok], z_ref[tok])
+    const float* mx;        // [R x nc32]
     float scale;            // loss scale
     int chunk;
-    int V, d, V_pad;
+    int V, d, V_pad, nc32;
     uint16_t* dS;           // [R x V_pad] scaled dlogits (without the 1/N_valid factor)
     uint16_t* dH;           // [N x d]
     float* dW;              // [V x d]
+    int* sched;             // zeroed work counter of this launch
     int* found_inf;
+    int* status;
+};
+
+struct MergeParams {
+    const float4* part;     // by row (chunk < 0) or by chunk slot
+    const float2* zt;
+    const uint8_t* mask;
+    const int* tokens;
+    const float* adv;
+    const int* counts;
+    const int* rows;        // chunk mode: valid-row list
+    int chunk;              // < 0: every row t in [0, N)
+    int R;                  // chunk rows (buffer height)
+    int S, L, V;
+    float beta;
+    int64_t N;
+    float* lse;
+    float* gco;
+    float* ell;
+    float* row_stats;
     int* status;
 };
 
 // ---- launches (return cudaError_t of the launch) ----
 cudaError_t launch_index(const uint8_t* mask, int64_t N, int R_max, int* counts, int* rows, int2* tiles,
-                         int* status, int* found_inf, cudaStream_t st);
+                         int* sched, int n_sched, int* status, cudaStream_t st);
 cudaError_t launch_advantages(const float* r, int n_groups, int G, float eps, int std_unbiased, float* adv,
                               cudaStream_t st);
 cudaError_t launch_build_mask(const int32_t* lengths, int n_seq, int L, uint8_t* mask, cudaStream_t st);
-cudaError_t launch_merge(const WsLayout& ws, char* wsp, const uint8_t* mask, const int* tokens,
-                         const float* adv, int L, int V, float beta, float* loss_out, float* row_stats,
-                         int* status, cudaStream_t st);
-cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, int R, cudaStream_t st);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, cudaStream_t st);
+cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, int nblk, const int* counts,
+                               float* loss_out, cudaStream_t st);
+cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
+                               cudaStream_t st);
+cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, cudaStream_t st);
 cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, cudaStream_t st);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st);
 

@@ -2,6 +2,8 @@
 // logsumexp merge + objective + deterministic loss, row gather and zeroing.
 #include <cfloat>
 #include <cmath>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 
@@ -125,13 +127,12 @@ __device__ __forceinline__ int block_excl_max(int v, int* s_warp, int* total) {
 
 __global__ void __launch_bounds__(kIndexThreads) k_index(const uint8_t* __restrict__ mask, int64_t N, int R_max,
                                                          int* __restrict__ counts, int* __restrict__ rows,
-                                                         int2* __restrict__ tiles, int* status, int* found_inf) {
+                                                         int2* __restrict__ tiles, int* __restrict__ sched,
+                                                         int n_sched, int* status) {
     __shared__ int s_warp[32];
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        *status = 0;
-        if (found_inf) *found_inf = 0;
-    }
+    if (tid == 0) *status = 0;
+    for (int i = tid; i < n_sched; i += kIndexThreads) sched[i] = 0;
     int carry_valid = 0, carry_tiles = 0, carry_lastzero = -1;
     for (int64_t base = 0; base < N; base += static_cast<int64_t>(kIndexThreads) * kItems) {
         const int t0 = static_cast<int>(base) + tid * kItems;
@@ -209,8 +210,8 @@ __global__ void k_tile_rows(const uint8_t* __restrict__ mask, int64_t N, const i
 }
 
 cudaError_t launch_index(const uint8_t* mask, int64_t N, int R_max, int* counts, int* rows, int2* tiles,
-                         int* status, int* found_inf, cudaStream_t st) {
-    k_index<<<1, kIndexThreads, 0, st>>>(mask, N, R_max, counts, rows, tiles, status, found_inf);
+                         int* sched, int n_sched, int* status, cudaStream_t st) {
+    k_index<<<1, kIndexThreads, 0, st>>>(mask, N, R_max, counts, rows, tiles, sched, n_sched, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     int blocks = static_cast<int>((N / kBM + 255) / 256) + 1;
@@ -237,48 +238,92 @@ __device__ __forceinline__ float merge_lse(const float4* __restrict__ part, int 
     return m + logf(acc);
 }
 
-__global__ void __launch_bounds__(kMergeThreads) k_merge(const float4* __restrict__ part, const float2* __restrict__ zt,
-                                                         int S, const uint8_t* __restrict__ mask,
-                                                         const int* __restrict__ tokens, const float* __restrict__ adv,
-                                                         int L, int V, float beta, int64_t N, float* __restrict__ lse_out,
-                                                         float* __restrict__ g_out, double* __restrict__ blocksum,
-                                                         float* __restrict__ row_stats, int* status) {
-    __shared__ double sh[kMergeThreads];
-    const int64_t t = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
-    double ell = 0.0;
-    if (t < N) {
-        float lse_p = 0.f, lse_r = 0.f, q = 0.f, p = 0.f, kl = 0.f, g = 0.f;
-        if (mask[t]) {
-            const int tok = tokens[t];
-            if (tok < 0 || tok >= V) {
-                atomicCAS(status, 0, GRPO_ERR_SHAPE);
-            } else {
-                const float4* pr = part + t * S;
-                lse_p = merge_lse(pr, S, false);
-                lse_r = merge_lse(pr, S, true);
-                const float2 z = zt[t];
-                q = z.x - lse_p;
-                p = z.y - lse_r;
-                const float x = p - q;
-                const float em1 = expm1f(x);
-                kl = em1 - x;
-                const float A = adv[t / L];
-                ell = static_cast<double>(-A + beta * kl);
-                g = -A - beta * em1;
-            }
-        }
-        lse_out[t] = lse_p;
-        g_out[t] = g;
-        if (row_stats) {
-            float* o = row_stats + t * 5;
-            o[0] = lse_p;
-            o[1] = lse_r;
-            o[2] = q;
-            o[3] = p;
-            o[4] = kl;
+// One thread per row: all rows t in [0, N) (chunk < 0), or the valid rows of
+// one backward chunk.  Writes lse_pol, g = d ell / d q and ell per row.
+__global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
+    int64_t t, pidx;
+    if (p.chunk < 0) {
+        t = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
+        if (t >= p.N) return;
+        pidx = t;
+    } else {
+        if (p.chunk >= p.counts[C_NCHUNKS]) return;
+        const int rc = p.counts[C_CHUNK_ROWS];
+        const int c0 = p.chunk * rc;
+        const int n_c = min(rc, p.counts[C_NVALID] - c0);
+        const int slot = blockIdx.x * kMergeThreads + threadIdx.x;
+        if (slot >= n_c) return;
+        t = p.rows[c0 + slot];
+        pidx = slot;
+    }
+    float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, kl = 0.f, g = 0.f, ell = 0.f;
+    if (p.mask[t]) {
+        const int tok = p.tokens[t];
+        if (tok < 0 || tok >= p.V) {
+            atomicCAS(p.status, 0, GRPO_ERR_SHAPE);
+        } else {
+            const float4* pr = p.part + pidx * p.S;
+            lse_p = merge_lse(pr, p.S, false);
+            lse_r = merge_lse(pr, p.S, true);
+            const float2 z = p.zt[t];
+            q = z.x - lse_p;
+            p_ = z.y - lse_r;
+            const float x = p_ - q;
+            const float em1 = expm1f(x);
+            kl = em1 - x;
+            const float A = p.adv[t / p.L];
+            ell = -A + p.beta * kl;
+            g = -A - p.beta * em1;
         }
     }
-    sh[threadIdx.x] = ell;
+    p.lse[t] = lse_p;
+    p.gco[t] = g;
+    p.ell[t] = ell;
+    if (p.row_stats) {
+        float* o = p.row_stats + t * 5;
+        o[0] = lse_p;
+        o[1] = lse_r;
+        o[2] = q;
+        o[3] = p_;
+        o[4] = kl;
+    }
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
+    const int64_t n = p.chunk < 0 ? p.N : static_cast<int64_t>(p.R);
+    int64_t blocks = (n + kMergeThreads - 1) / kMergeThreads;
+    if (blocks < 1) blocks = 1;
+    k_merge<<<static_cast<unsigned>(blocks), kMergeThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// masked rows: objective 0 and zero diagnostics (the chunked merge never visits them)
+__global__ void k_rows_init(const uint8_t* __restrict__ mask, int64_t N, float* __restrict__ ell,
+                            float* __restrict__ row_stats) {
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < N;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        if (mask[t]) continue;
+        ell[t] = 0.f;
+        if (row_stats)
+            for (int j = 0; j < 5; ++j) row_stats[t * 5 + j] = 0.f;
+    }
+}
+
+cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, cudaStream_t st) {
+    int blocks = static_cast<int>((N + 255) / 256);
+    if (blocks > 2048) blocks = 2048;
+    if (blocks < 1) blocks = 1;
+    k_rows_init<<<blocks, 256, 0, st>>>(mask, N, ell, row_stats);
+    return cudaGetLastError();
+}
+
+// Masked mean of the per-row objective: fp64 sums over fixed blocks of rows in
+// a fixed tree, then one block sums the block results in a fixed order.
+__global__ void __launch_bounds__(kMergeThreads) k_loss_blocks(const float* __restrict__ ell, int64_t N,
+                                                               double* __restrict__ blocksum) {
+    __shared__ double sh[kMergeThreads];
+    const int64_t t = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
+    sh[threadIdx.x] = t < N ? static_cast<double>(ell[t]) : 0.0;
     __syncthreads();
 #pragma unroll
     for (int s = kMergeThreads / 2; s > 0; s >>= 1) {
@@ -305,25 +350,22 @@ __global__ void __launch_bounds__(1024) k_loss_final(const double* __restrict__ 
     }
 }
 
-cudaError_t launch_merge(const WsLayout& ws, char* wsp, const uint8_t* mask, const int* tokens, const float* adv,
-                         int L, int V, float beta, float* loss_out, float* row_stats, int* status,
-                         cudaStream_t st) {
-    k_merge<<<ws.nblk, kMergeThreads, 0, st>>>(
-        reinterpret_cast<const float4*>(wsp + ws.part), reinterpret_cast<const float2*>(wsp + ws.zt), ws.S, mask,
-        tokens, adv, L, V, beta, ws.N, reinterpret_cast<float*>(wsp + ws.lse), reinterpret_cast<float*>(wsp + ws.gco),
-        reinterpret_cast<double*>(wsp + ws.blocksum), row_stats, status);
+cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, int nblk, const int* counts,
+                               float* loss_out, cudaStream_t st) {
+    k_loss_blocks<<<nblk, kMergeThreads, 0, st>>>(ell, N, blocksum);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_loss_final<<<1, 1024, 0, st>>>(reinterpret_cast<const double*>(wsp + ws.blocksum), ws.nblk,
-                                     reinterpret_cast<const int*>(wsp + ws.counts), loss_out);
+    k_loss_final<<<1, 1024, 0, st>>>(blocksum, nblk, counts, loss_out);
     return cudaGetLastError();
 }
 
 // ------------------------------------------------------------ gather / zero
-// Hc[slot] = h_pol[rows[c0 + slot]] for the chunk's slots; the slots after
-// the last one, up to the next multiple of kBM, are zeroed.
+// Hc[slot] = h_pol[rows[c0 + slot]] (and Hcr from h_ref when given) for the
+// chunk's slots; the slots after the last one, up to the next multiple of kBM,
+// are zeroed.
 __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restrict__ rows, int chunk,
-                              const uint4* __restrict__ h, uint4* __restrict__ hc, int vec_per_row, int R) {
+                              const uint4* __restrict__ h, uint4* __restrict__ hc, const uint4* __restrict__ hr,
+                              uint4* __restrict__ hcr, int vec_per_row, int R) {
     if (chunk >= counts[C_NCHUNKS]) return;
     const int rc = counts[C_CHUNK_ROWS];
     const int c0 = chunk * rc;
@@ -334,19 +376,98 @@ __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restr
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int slot = static_cast<int>(i / vec_per_row);
         const int v = static_cast<int>(i - static_cast<int64_t>(slot) * vec_per_row);
-        uint4 x = make_uint4(0, 0, 0, 0);
-        if (slot < n_c) x = h[static_cast<int64_t>(rows[c0 + slot]) * vec_per_row + v];
+        uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
+        if (slot < n_c) {
+            const int64_t src = static_cast<int64_t>(rows[c0 + slot]) * vec_per_row + v;
+            x = h[src];
+            if (hr) y = hr[src];
+        }
         hc[i] = x;
+        if (hcr) hcr[i] = y;
     }
 }
 
-cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, int R, cudaStream_t st) {
+cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
+                               cudaStream_t st) {
     const int vpr = p.d / 8;
     const int64_t total = static_cast<int64_t>(R) * vpr;
     int blocks = static_cast<int>((total + 255) / 256);
-    if (blocks > 148 * 16) blocks = 148 * 16;
+    if (blocks > 152 * 16) blocks = 152 * 16;
     k_gather_rows<<<blocks, 256, 0, st>>>(p.counts, p.rows, p.chunk, static_cast<const uint4*>(h_pol),
-                                          static_cast<uint4*>(hc), vpr, R);
+                                          static_cast<uint4*>(hc), static_cast<const uint4*>(h_ref),
+                                          static_cast<uint4*>(hcr), vpr, R);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ dlogits from stored exponentials
+// In place over the chunk buffer: the forward left e = exp(z - m) (bf16) for
+// every policy logit and m, the running max after each 32-column group.  With
+// the row's logsumexp the softmax is p = e * exp(m - lse), and
+//   dS = s * g * (onehot(tok) - p)
+// is written back in the storage dtype.  The sampled token's entry uses
+// p_tok = exp(z[tok] - lse) in fp32, so 1 - p_tok keeps full precision.
+// Slots past the chunk's last row (to the next multiple of kBM) become 0.
+template <bool kBf16>
+__global__ void __launch_bounds__(kTransformThreads) k_transform(const ChunkParams p, int R) {
+    if (p.chunk >= p.counts[C_NCHUNKS]) return;
+    const int rc = p.counts[C_CHUNK_ROWS];
+    const int c0 = p.chunk * rc;
+    const int n_c = min(rc, p.counts[C_NVALID] - c0);
+    const int n_fill = min(R, (n_c + kBM - 1) / kBM * kBM);
+    const int nvec = (p.V + 7) / 8;   // 8 elements (16 bytes) per vector; V_pad is a multiple of 64
+    bool bad = false;
+    for (int slot = blockIdx.x; slot < n_fill; slot += gridDim.x) {
+        uint4* row = reinterpret_cast<uint4*>(p.dS + static_cast<int64_t>(slot) * p.V_pad);
+        if (slot >= n_c) {
+            for (int i = threadIdx.x; i < nvec; i += kTransformThreads) row[i] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const int t = p.rows[c0 + slot];
+        const int tok = p.tokens[t];
+        const float lse = p.lse[t];
+        const float coef = p.scale * p.gco[t];
+        const float ptok = expf(p.zt[t].x - lse);
+        const float* mrow = p.mx + static_cast<int64_t>(slot) * p.nc32;
+        for (int i = threadIdx.x; i < nvec; i += kTransformThreads) {
+            const int v0 = i * 8;
+            const float c = coef * expf(mrow[v0 >> 5] - lse);
+            uint4 u = row[i];
+            uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float e0 = __uint_as_float(w[j] << 16);
+                const float e1 = __uint_as_float(w[j] & 0xFFFF0000u);
+                const int va = v0 + 2 * j, vb = va + 1;
+                float d0 = -c * e0, d1 = -c * e1;
+                if (va == tok) d0 = coef * (1.f - ptok);
+                if (vb == tok) d1 = coef * (1.f - ptok);
+                if (va >= p.V) d0 = 0.f;
+                if (vb >= p.V) d1 = 0.f;
+                uint16_t h0, h1;
+                if (kBf16) {
+                    h0 = __bfloat16_as_ushort(__float2bfloat16_rn(d0));
+                    h1 = __bfloat16_as_ushort(__float2bfloat16_rn(d1));
+                } else {
+                    h0 = __half_as_ushort(__float2half_rn(d0));
+                    h1 = __half_as_ushort(__float2half_rn(d1));
+                    bad |= ((h0 & 0x7C00u) == 0x7C00u) || ((h1 & 0x7C00u) == 0x7C00u);
+                }
+                o[j] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+            }
+            row[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    if (!kBf16 && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.found_inf, 1);
+}
+
+cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, cudaStream_t st) {
+    int blocks = R;
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (bf16)
+        k_transform<true><<<blocks, kTransformThreads, 0, st>>>(p, R);
+    else
+        k_transform<false><<<blocks, kTransformThreads, 0, st>>>(p, R);
     return cudaGetLastError();
 }
 

@@ -43,6 +43,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t a) { return make_sdesc_sw128(a, 16, 1024); }
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t a) { return make_sdesc_sw128(a, 8192, 1024); }
 
+constexpr int kUnitSlots = 4;   // work units published ahead by the producer
+
 struct Smem {
     uint8_t* stages;
     uint64_t* full;
@@ -50,8 +52,11 @@ struct Smem {
     uint64_t* acc_full;
     uint64_t* acc_empty;
     uint64_t* drain;
+    uint64_t* unit_full;
+    uint64_t* unit_empty;
     uint32_t* tmem_slot;
     volatile int* abort_flag;
+    volatile int* unit_id;
 };
 
 template <int kStages, int kStageBytes>
@@ -65,8 +70,11 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     s.acc_full = s.empty + kStages;
     s.acc_empty = s.acc_full + 2;
     s.drain = s.acc_empty + 2;
-    s.tmem_slot = reinterpret_cast<uint32_t*>(s.drain + 1);
+    s.unit_full = s.drain + 1;
+    s.unit_empty = s.unit_full + kUnitSlots;
+    s.tmem_slot = reinterpret_cast<uint32_t*>(s.unit_empty + kUnitSlots);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
+    s.unit_id = s.abort_flag + 1;
     return s;
 }
 
@@ -108,20 +116,34 @@ struct FwdT {
     using Params = FwdParams;
     struct Sched {
         int n_units, ks, n_tiles, C;
+        int c0, n_c;           // chunk mode: first valid-row index and rows of the chunk
+        bool chunked;
     };
     struct Coord {
         int t0, n0;
     };
     struct Epi {
         float m[2], s[2], zt[2];
-        int tok, t, split;
+        int tok, t, split, slot;
         bool valid, found;
     };
 
-    // unit = tile group * S + split; the tile of rank r is group * C + r
+    // unit = tile group * S + split; the tile of rank r is group * C + r.
+    // Tile mode: forward row tiles over h_pol/h_ref.  Chunk mode: 128-row tiles
+    // of the chunk's compact copies.
     __device__ static bool setup(const Params& p, Sched& sc, int C) {
         sc.C = C;
-        sc.n_tiles = p.counts[C_NTILES];
+        sc.chunked = p.tiles == nullptr;
+        if (sc.chunked) {
+            if (p.chunk >= p.counts[C_NCHUNKS]) return false;
+            const int rc = p.counts[C_CHUNK_ROWS];
+            sc.c0 = p.chunk * rc;
+            sc.n_c = min(rc, p.counts[C_NVALID] - sc.c0);
+            sc.n_tiles = (sc.n_c + kBM - 1) / kBM;
+        } else {
+            sc.c0 = sc.n_c = 0;
+            sc.n_tiles = p.counts[C_NTILES];
+        }
         sc.n_units = ((sc.n_tiles + C - 1) / C) * p.S;
         sc.ks = p.d / kBK;
         return sc.n_units > 0;
@@ -139,7 +161,10 @@ struct FwdT {
     __device__ static Coord coord(const Params& p, const Sched& sc, int unit, int item, int rank) {
         Coord c;
         const int tile = tile_of(p, sc, unit, rank);
-        c.t0 = tile < sc.n_tiles ? p.tiles[tile].x : static_cast<int>(p.N);   // phantom: rows past the end
+        if (sc.chunked)
+            c.t0 = tile * kBM;
+        else
+            c.t0 = tile < sc.n_tiles ? p.tiles[tile].x : static_cast<int>(p.N);   // phantom: rows past the end
         c.n0 = ((unit % p.S) * p.nps + item) * kBN;
         return c;
     }
@@ -170,7 +195,15 @@ struct FwdT {
         const int tile = tile_of(p, sc, unit, rank);
         e.valid = false;
         e.t = 0;
-        if (tile < sc.n_tiles) {
+        e.slot = -1;
+        if (sc.chunked) {
+            const int slot = tile * kBM + row;
+            if (slot < sc.n_c) {
+                e.valid = true;
+                e.slot = slot;
+                e.t = p.rows[sc.c0 + slot];
+            }
+        } else if (tile < sc.n_tiles) {
             const int2 tl = p.tiles[tile];
             e.t = tl.x + row;
             e.valid = row < tl.y;
@@ -183,8 +216,13 @@ struct FwdT {
         e.found = false;
     }
     template <bool kBf16>
-    __device__ static void epi_item(const Params& p, const Sched&, int unit, int item, int, uint32_t tacc, Epi& e) {
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int item, int, uint32_t tacc,
+                                    Epi& e) {
         const int n0 = ((unit % p.S) * p.nps + item) * kBN;
+        // chunk mode keeps the policy exponentials for the backward
+        const bool keep = sc.chunked && p.E != nullptr && e.valid;
+        uint16_t* erow = keep ? p.E + static_cast<int64_t>(e.slot) * p.V_pad : nullptr;
+        float* mrow = keep ? p.mx + static_cast<int64_t>(e.slot) * p.nc32 : nullptr;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
 #pragma unroll 1
@@ -204,11 +242,6 @@ struct FwdT {
                 for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
                 const float m_new = fmaxf(e.m[w], cmax);
                 const float mb = m_new * kLog2e;
-                float acc = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc += fast_exp2(fmaf(v[j], kLog2e, -mb));
-                e.s[w] = fmaf(e.s[w], fast_exp2(fmaf(e.m[w], kLog2e, -mb)), acc);
-                e.m[w] = m_new;
                 const bool hit = static_cast<unsigned>(e.tok - col0) < 32u;
                 if (__any_sync(0xffffffffu, hit)) {
 #pragma unroll
@@ -216,12 +249,30 @@ struct FwdT {
                         if (e.tok == col0 + j) e.zt[w] = v[j];
                     if (hit) e.found = true;
                 }
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = fast_exp2(fmaf(v[j], kLog2e, -mb));
+                    acc += v[j];
+                }
+                e.s[w] = fmaf(e.s[w], fast_exp2(fmaf(e.m[w], kLog2e, -mb)), acc);
+                e.m[w] = m_new;
+                if (w == 0 && keep) {
+                    uint4* o4 = reinterpret_cast<uint4*>(erow + col0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        o4[j] = make_uint4(pack2(v[8 * j], v[8 * j + 1], true), pack2(v[8 * j + 2], v[8 * j + 3], true),
+                                           pack2(v[8 * j + 4], v[8 * j + 5], true),
+                                           pack2(v[8 * j + 6], v[8 * j + 7], true));
+                    mrow[col0 >> 5] = m_new;
+                }
             }
         }
     }
-    __device__ static void epi_end(const Params& p, const Sched&, int, Epi& e) {
+    __device__ static void epi_end(const Params& p, const Sched& sc, int, Epi& e) {
         if (!e.valid) return;
-        p.part[static_cast<int64_t>(e.t) * p.S + e.split] = make_float4(e.m[0], e.s[0], e.m[1], e.s[1]);
+        const int64_t idx = sc.chunked ? static_cast<int64_t>(e.slot) : static_cast<int64_t>(e.t);
+        p.part[idx * p.S + e.split] = make_float4(e.m[0], e.s[0], e.m[1], e.s[1]);
         if (e.found) p.zt[e.t] = make_float2(e.zt[0], e.zt[1]);
     }
 };
@@ -534,6 +585,8 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     if (cid >= sc.n_units) return;   // no work for this cluster: leave before touching TMEM
     const int rank = kC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
     constexpr uint16_t kMask = static_cast<uint16_t>((1u << kC) - 1u);
+    // single CTAs take units from a per-launch counter; clusters walk a fixed stride
+    int* const sched = kC == 1 ? p.sched : nullptr;
 
     Smem sm = carve_smem<T::kStages, T::kStageBytes>(smem_raw);
     const int warp = threadIdx.x >> 5;
@@ -548,6 +601,10 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.acc_full[b], 1);
             mbar_init(&sm.acc_empty[b], 4);
+        }
+        for (int u = 0; u < kUnitSlots; ++u) {
+            mbar_init(&sm.unit_full[u], 1);
+            mbar_init(&sm.unit_empty[u], 5);   // the MMA lane and the four epilogue warps
         }
         mbar_init(sm.drain, 1);
         *sm.abort_flag = 0;
@@ -572,9 +629,26 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            for (int unit = cid; unit < sc.n_units; unit += n_clusters) {
+            int s = 0, us = 0;
+            uint32_t ph = 0, uph = 0;
+            int next = cid;
+            while (true) {
+                int unit;
+                if (sched) {
+                    unit = atomicAdd(sched, 1);
+                } else {
+                    unit = next;
+                    next += n_clusters;
+                }
+                // publish the unit to the MMA and epilogue roles
+                if (!mbar_wait(&sm.unit_empty[us], uph ^ 1u, sm.abort_flag, status)) goto producer_done;
+                sm.unit_id[us] = unit;
+                mbar_arrive(&sm.unit_full[us]);
+                if (++us == kUnitSlots) {
+                    us = 0;
+                    uph ^= 1u;
+                }
+                if (unit >= sc.n_units) break;
                 const int n_items = T::items(p, sc, unit);
                 const int ks = T::ksteps(p, sc, unit);
                 for (int item = 0; item < n_items; ++item) {
@@ -599,10 +673,18 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
+            int s = 0, us = 0;
+            uint32_t ph = 0, uph = 0;
             int it = 0;
-            for (int unit = cid; unit < sc.n_units; unit += n_clusters) {
+            while (true) {
+                if (!mbar_wait(&sm.unit_full[us], uph, sm.abort_flag, status)) goto mma_done;
+                const int unit = sm.unit_id[us];
+                mbar_arrive(&sm.unit_empty[us]);
+                if (++us == kUnitSlots) {
+                    us = 0;
+                    uph ^= 1u;
+                }
+                if (unit >= sc.n_units) break;
                 const int n_items = T::items(p, sc, unit);
                 const int ks = T::ksteps(p, sc, unit);
                 for (int item = 0; item < n_items; ++item, ++it) {
@@ -646,8 +728,18 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
         // ------------------------------------------------ epilogue
         const int row = lane + 32 * (warp & 3);
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-        int it = 0;
-        for (int unit = cid; unit < sc.n_units; unit += n_clusters) {
+        int it = 0, us = 0;
+        uint32_t uph = 0;
+        while (true) {
+            if (!mbar_wait(&sm.unit_full[us], uph, sm.abort_flag, status)) goto epi_done;
+            const int unit = sm.unit_id[us];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.unit_empty[us]);
+            if (++us == kUnitSlots) {
+                us = 0;
+                uph ^= 1u;
+            }
+            if (unit >= sc.n_units) break;
             const int n_items = T::items(p, sc, unit);
             typename T::Epi e;
             T::epi_begin(p, sc, unit, rank, row, e);

@@ -182,19 +182,26 @@ def test_fp16_overflow_sets_found_inf_and_halving_recovers():
     assert_grad_parity(res, exp, loss_scale=scale)
 
 
-def test_deterministic_and_fwd_equals_fwd_bwd():
+def test_deterministic_and_fwd_matches_fwd_bwd():
     cfg = synth.make_config("tiny", G=4, L=300, d=256, V=3000)
     wl = synth.generate(cfg, seed=13)
     dw = DeviceWorkload(wl, chunk_rows=256)
     dw.fwd()
     loss_fwd = dw.loss.clone()
     stats_fwd = dw.row_stats.clone()
+    dw.fwd()
+    assert torch.equal(loss_fwd.view(torch.int32), dw.loss.view(torch.int32))
+    assert torch.equal(stats_fwd, dw.row_stats)
     dw.fwd_bwd()
     a = {k: v.clone() for k, v in (("loss", dw.loss), ("dH", dw.dH), ("dW", dw.dW), ("rs", dw.row_stats))}
     dw.fwd_bwd()
-    assert torch.equal(loss_fwd.view(torch.int32), a["loss"].view(torch.int32))
-    assert torch.equal(stats_fwd, a["rs"])
+    # the two entry points split the vocabulary differently: equal up to fp32 rounding
+    lf, lb = float(loss_fwd.item()), float(a["loss"].item())
+    assert abs(lf - lb) <= 1e-6 * max(abs(lf), 1e-30)
+    assert torch.allclose(stats_fwd, a["rs"], rtol=1e-6, atol=1e-6)
+    # every entry point is bitwise reproducible
     assert torch.equal(a["loss"].view(torch.int32), dw.loss.view(torch.int32))
+    assert torch.equal(a["rs"], dw.row_stats)
     assert torch.equal(a["dH"].view(torch.int16), dw.dH.view(torch.int16))
     assert torch.equal(a["dW"].view(torch.int32), dw.dW.view(torch.int32))
 
