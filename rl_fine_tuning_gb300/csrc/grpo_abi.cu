@@ -433,7 +433,8 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     void* hc = w + L.hc;
     void* hcr = w + L.hcr;
     void* ds = w + L.ds;
-    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterFwd) ||
+    // W tiles for the pair forward: each CTA of a pair loads 128 of the 256 vocabulary rows
+    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN / 2) ||
         !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) || !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
         !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
         !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
@@ -478,16 +479,16 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
         if (launch(GRPO_PROF_GATHER, st, [&] { return launch_gather_rows(cp, h_pol, hc, h_ref, hcr, L.R, st); }) !=
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_FWD, st, [&] { return launch_fwd(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) !=
-            cudaSuccess)
+        if (launch(GRPO_PROF_FWD, st,
+                   [&] { return launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_DS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DH, st, [&] { return launch_dh(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
+        if (launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DW, st, [&] { return launch_dw(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st); }) !=
+        if (launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st); }) !=
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
     }

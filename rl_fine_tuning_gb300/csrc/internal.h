@@ -124,6 +124,13 @@ cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void*
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
                        const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
+// CTA-pair (M=256) variants: forward of a chunk, dH, dW
+cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
+                            const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
+cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm,
+                           bool bf16, cudaStream_t st);
+cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
+                           bool bf16, cudaStream_t st);
 cudaError_t launch_ds(const ChunkParams& p, const CUtensorMap& mHc, const CUtensorMap& mW, int n_sm, bool bf16,
                       cudaStream_t st);
 cudaError_t launch_dh(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm,

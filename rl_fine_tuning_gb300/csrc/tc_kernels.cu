@@ -769,6 +769,479 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     }
 }
 
+// ====================================================================== CTA-pair kernels
+// The same stages on pairs of SMs with M=256 tcgen05 MMAs (cta_group::2): each
+// CTA of a pair holds its own 128-row A tile and half of the 256-column B
+// tile, so per SM a K-stage is 32 KB of shared memory instead of 48-64 KB, and
+// its tensor memory holds a double-buffered 128x256 accumulator.
+
+// 128-row tiles of a chunk visited group by group: all splits of a group of
+// kFwdGroup tiles run together, so W streams from L2 once per group.
+constexpr int kFwdGroup = 8;
+
+__device__ __forceinline__ void decode_tile_split(int unit, int n_mt, int S, int* mt, int* split) {
+    const int full = (n_mt / kFwdGroup) * kFwdGroup;
+    if (unit < full * S) {
+        const int gi = unit / (kFwdGroup * S);
+        const int r = unit - gi * kFwdGroup * S;
+        *split = r / kFwdGroup;
+        *mt = gi * kFwdGroup + (r - *split * kFwdGroup);
+    } else {
+        const int u2 = unit - full * S;
+        const int g_last = n_mt - full;
+        *split = u2 / g_last;
+        *mt = full + (u2 - *split * g_last);
+    }
+}
+
+// Forward of one chunk: the leader's A rows are the policy tile, the peer's the
+// reference tile of the same 128 compact rows; the leader also keeps the
+// policy exponentials for the backward.
+struct FwdPairT {
+    static constexpr int kStages = 6;
+    static constexpr int kStageBytes = 16384 + 16384;   // A (128x64), B half (128x64)
+    using Params = FwdParams;
+    struct Sched {
+        int n_units, ks, n_mt, c0, n_c;
+    };
+    struct Coord {
+        int m0, n0;
+    };
+    struct Epi {
+        float m, s, zt;
+        int tok, t, split, slot;
+        bool valid, found;
+    };
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (p.chunk >= p.counts[C_NCHUNKS]) return false;
+        const int rc = p.counts[C_CHUNK_ROWS];
+        sc.c0 = p.chunk * rc;
+        sc.n_c = min(rc, p.counts[C_NVALID] - sc.c0);
+        sc.n_mt = (sc.n_c + kBM - 1) / kBM;
+        sc.n_units = sc.n_mt * p.S;
+        sc.ks = p.d / kBK;
+        return sc.n_units > 0;
+    }
+    __device__ static int items(const Params& p, const Sched& sc, int unit) {
+        int mt, split;
+        decode_tile_split(unit, sc.n_mt, p.S, &mt, &split);
+        const int nb = split * p.nps;
+        return max(min(nb + p.nps, p.n_ntiles) - nb, 0);
+    }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params& p, const Sched& sc, int unit, int item, int) {
+        int mt, split;
+        decode_tile_split(unit, sc.n_mt, p.S, &mt, &split);
+        return Coord{mt * kBM, (split * p.nps + item) * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params&, const Sched&, const Coord&) { return 2 * kStageBytes; }
+    __device__ static void load(const Params&, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap* mA2, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(rank == 0 ? mA : mA2, bar, st, k * kBK, c.m0);
+        tma_load_2d_pair(mB, bar, st + 16384, k * kBK, c.n0 + rank * 128);
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(256, 256, kBf16, false, false);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_pair_f16(acc, desc_kmajor(st + kk * 32), desc_kmajor(st + 16384 + kk * 32), idesc,
+                          (first && kk == 0) ? 0u : 1u);
+    }
+    __device__ static void epi_begin(const Params& p, const Sched& sc, int unit, int, int row, Epi& e) {
+        int mt, split;
+        decode_tile_split(unit, sc.n_mt, p.S, &mt, &split);
+        e.slot = mt * kBM + row;
+        e.valid = e.slot < sc.n_c;
+        e.t = e.valid ? p.rows[sc.c0 + e.slot] : 0;
+        e.tok = e.valid ? p.tokens[e.t] : -1;
+        e.split = split;
+        e.m = -INFINITY;
+        e.s = 0.f;
+        e.zt = 0.f;
+        e.found = false;
+    }
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched&, int unit, int item, int rank, uint32_t tacc,
+                                    Epi& e) {
+        const int n0 = (e.split * p.nps + item) * kBN;
+        (void)unit;
+        const bool keep = rank == 0 && p.E != nullptr && e.valid;
+        uint16_t* erow = keep ? p.E + static_cast<int64_t>(e.slot) * p.V_pad : nullptr;
+        float* mrow = keep ? p.mx + static_cast<int64_t>(e.slot) * p.nc32 : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.V) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            const int nvalid = p.V - col0;
+            if (nvalid < 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j >= nvalid) v[j] = -INFINITY;
+            }
+            float cmax = v[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+            const float m_new = fmaxf(e.m, cmax);
+            const float mb = m_new * kLog2e;
+            const bool hit = static_cast<unsigned>(e.tok - col0) < 32u;
+            if (__any_sync(0xffffffffu, hit)) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (e.tok == col0 + j) e.zt = v[j];
+                if (hit) e.found = true;
+            }
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                v[j] = fast_exp2(fmaf(v[j], kLog2e, -mb));
+                acc += v[j];
+            }
+            e.s = fmaf(e.s, fast_exp2(fmaf(e.m, kLog2e, -mb)), acc);
+            e.m = m_new;
+            if (keep) {
+                uint4* o4 = reinterpret_cast<uint4*>(erow + col0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    o4[j] = make_uint4(pack2(v[8 * j], v[8 * j + 1], true), pack2(v[8 * j + 2], v[8 * j + 3], true),
+                                       pack2(v[8 * j + 4], v[8 * j + 5], true), pack2(v[8 * j + 6], v[8 * j + 7], true));
+                mrow[col0 >> 5] = m_new;
+            }
+        }
+    }
+    // the leader writes the policy half of the partials, the peer the reference half
+    __device__ static void epi_end(const Params& p, const Sched&, int rank, Epi& e) {
+        if (!e.valid) return;
+        float* part = reinterpret_cast<float*>(p.part + static_cast<int64_t>(e.slot) * p.S + e.split);
+        *reinterpret_cast<float2*>(part + 2 * rank) = make_float2(e.m, e.s);
+        if (e.found) reinterpret_cast<float*>(p.zt + e.t)[rank] = e.zt;
+    }
+};
+
+struct DhPairT {
+    static constexpr int kStages = 6;
+    static constexpr int kStageBytes = 16384 + 16384;   // A (128 slots x 64 vocab), B half (64 vocab x 128 d)
+    using Params = ChunkParams;
+    using Sched = ChunkSched;
+    struct Coord {
+        int m0, n0;
+    };
+    struct Epi {
+        int unused;
+    };
+    // unit = m-pair * n_nt + d-tile; the CTA of rank r takes m-tile 2*pair + r
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!chunk_setup(p, sc, 2)) return false;
+        sc.n_nt = (p.d + kBN - 1) / kBN;
+        sc.n_g = (sc.n_mt + 1) / 2;
+        sc.ks = (p.V + kBK - 1) / kBK;
+        sc.n_units = sc.n_g * sc.n_nt;
+        return true;
+    }
+    __device__ static int mtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * 2 + rank; }
+    __device__ static int items(const Params&, const Sched&, int) { return 1; }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
+        return Coord{mtile(sc, unit, rank) * kBM, (unit % sc.n_nt) * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
+        return 2 * 16384 + 8192 * min(4, (p.d - c.n0) / 64);
+    }
+    __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(mA, bar, st, k * kBK, c.m0);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = c.n0 + rank * 128 + 64 * j;
+            if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384 + 8192 * j, col, k * kBK);
+        }
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(256, 256, kBf16, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_pair_f16(acc, desc_kmajor(st + kk * 32), desc_mnmajor(st + 16384 + kk * 2048), idesc,
+                          (first && kk == 0) ? 0u : 1u);
+    }
+    __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int slot = mtile(sc, unit, rank) * kBM + row;
+        const int n0 = (unit % sc.n_nt) * kBN;
+        const bool valid = slot < sc.n_c;
+        if (!__any_sync(0xffffffffu, valid)) return;
+        const int t = valid ? p.rows[sc.c0 + slot] : 0;
+        uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
+        bool bad = false;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2(v[j] * sc.winv, v[j + 1] * sc.winv, kBf16);
+            if (!kBf16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
+            }
+            if (valid) {
+                uint4* o4 = reinterpret_cast<uint4*>(out + col0);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+        }
+        if (bad && valid) atomicOr(p.found_inf, 1);
+    }
+    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
+};
+
+struct DwPairT {
+    static constexpr int kStages = 6;
+    static constexpr int kStageBytes = 16384 + 16384;   // A (64 slots x 128 vocab), B half (64 slots x 128 d)
+    using Params = ChunkParams;
+    using Sched = ChunkSched;
+    struct Coord {
+        int v0, n0;
+    };
+    struct Epi {
+        int unused;
+    };
+    // unit = vocab-pair * n_nt + d-tile; the CTA of rank r takes vocabulary tile 2*pair + r
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!chunk_setup(p, sc, 2)) return false;
+        sc.n_nt = (p.d + kBN - 1) / kBN;
+        sc.n_g = ((p.V + kBM - 1) / kBM + 1) / 2;
+        sc.ks = (sc.n_c + kBK - 1) / kBK;
+        sc.n_units = sc.n_g * sc.n_nt;
+        return true;
+    }
+    __device__ static int vtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * 2 + rank; }
+    __device__ static int items(const Params&, const Sched&, int) { return 1; }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
+        return Coord{vtile(sc, unit, rank) * kBM, (unit % sc.n_nt) * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
+        return 2 * 16384 + 8192 * min(4, (p.d - c.n0) / 64);
+    }
+    __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(mA, bar, st, c.v0, k * kBK);
+        tma_load_2d_pair(mA, bar, st + 8192, c.v0 + 64, k * kBK);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = c.n0 + rank * 128 + 64 * j;
+            if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384 + 8192 * j, col, k * kBK);
+        }
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(256, 256, kBf16, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_pair_f16(acc, desc_mnmajor(st + kk * 2048), desc_mnmajor(st + 16384 + kk * 2048), idesc,
+                          (first && kk == 0) ? 0u : 1u);
+    }
+    __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int v = vtile(sc, unit, rank) * kBM + row;
+        const int n0 = (unit % sc.n_nt) * kBN;
+        const bool valid = v < p.V;
+        if (!__any_sync(0xffffffffu, valid)) return;
+        const bool first_chunk = p.chunk == 0;
+        float* out = p.dW + static_cast<int64_t>(valid ? v : 0) * p.d;
+        bool bad = false;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float x[32];
+            tmem_ld32(tacc + c * 32, x);
+            if (valid) {
+                float4* o4 = reinterpret_cast<float4*>(out + col0);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float4 r = make_float4(x[4 * j] * sc.winv, x[4 * j + 1] * sc.winv, x[4 * j + 2] * sc.winv,
+                                           x[4 * j + 3] * sc.winv);
+                    if (!first_chunk) {
+                        const float4 o = o4[j];
+                        r.x += o.x;
+                        r.y += o.y;
+                        r.z += o.z;
+                        r.w += o.w;
+                    }
+                    bad |= !(isfinite(r.x) && isfinite(r.y) && isfinite(r.z) && isfinite(r.w));
+                    o4[j] = r;
+                }
+            }
+        }
+        if (bad) atomicOr(p.found_inf, 1);
+    }
+    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
+};
+
+template <class T, bool kBf16>
+__device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const CUtensorMap& mA, const CUtensorMap& mA2,
+                                             const CUtensorMap& mB) {
+    extern __shared__ uint8_t smem_raw[];
+    typename T::Sched sc;
+    // uniform across the pair: both CTAs read the same counters
+    if (!T::setup(p, sc)) return;
+    const int cid = static_cast<int>(blockIdx.x) >> 1;
+    const int n_pairs = static_cast<int>(gridDim.x) >> 1;
+    if (cid >= sc.n_units) return;   // no work for this pair: leave before touching TMEM
+    const int rank = static_cast<int>(cluster_ctarank());
+    const bool leader = rank == 0;
+
+    Smem sm = carve_smem<T::kStages, T::kStageBytes>(smem_raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int* status = p.status;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::kStages; ++s) {
+            mbar_init(&sm.full[s], 1);    // leader: its producer's expect_tx + both CTAs' bytes
+            mbar_init(&sm.empty[s], 1);   // the leader's MMA commit, multicast to both CTAs
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.acc_full[b], 1);    // the leader's commit, multicast
+            mbar_init(&sm.acc_empty[b], 8);   // leader: the epilogue warps of both CTAs
+        }
+        mbar_init(sm.drain, 1);
+        *sm.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&mA);
+        tma_prefetch_desc(&mA2);
+        tma_prefetch_desc(&mB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(sm.tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = *sm.tmem_slot;
+    const uint32_t full0 = map_cluster(smem_u32(&sm.full[0]), 0);
+    const uint32_t acc_empty0 = map_cluster(smem_u32(&sm.acc_empty[0]), 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            for (int unit = cid; unit < sc.n_units; unit += n_pairs) {
+                const int n_items = T::items(p, sc, unit);
+                const int ks = T::ksteps(p, sc, unit);
+                for (int item = 0; item < n_items; ++item) {
+                    const typename T::Coord c = T::coord(p, sc, unit, item, rank);
+                    const uint32_t bytes = T::tx_bytes(p, sc, c);
+                    for (int k = 0; k < ks; ++k) {
+                        if (!mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, status)) goto producer_done;
+                        if (leader) mbar_arrive_expect_tx(&sm.full[s], bytes);
+                        T::load(p, sc, c, k, sm.stages + s * T::kStageBytes, full0 + 8u * s, &mA, &mA2, &mB, rank);
+                        if (++s == T::kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (lane == 0 && leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            int it = 0;
+            for (int unit = cid; unit < sc.n_units; unit += n_pairs) {
+                const int n_items = T::items(p, sc, unit);
+                const int ks = T::ksteps(p, sc, unit);
+                for (int item = 0; item < n_items; ++item, ++it) {
+                    const int b = it & 1;
+                    const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+                    if (!mbar_wait(&sm.acc_empty[b], aph ^ 1u, sm.abort_flag, status)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t acc = tmem + b * 256;
+                    for (int k = 0; k < ks; ++k) {
+                        if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, status)) goto mma_done;
+                        tc_fence_after();
+                        T::template mma<kBf16>(smem_u32(sm.stages + s * T::kStageBytes), acc, k == 0);
+                        umma_pair_commit_both(&sm.empty[s]);
+                        if (++s == T::kStages) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    umma_pair_commit_both(&sm.acc_full[b]);
+                }
+            }
+        mma_done:
+            umma_pair_commit(sm.drain);
+            {
+                const uint32_t a = smem_u32(sm.drain);
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(a, 0)) {
+                    if (globaltimer() - t0 > kWaitTimeoutNs) {
+                        atomicCAS(status, 0, GRPO_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (both CTAs, own rows)
+        const int row = lane + 32 * (warp & 3);
+        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+        int it = 0;
+        for (int unit = cid; unit < sc.n_units; unit += n_pairs) {
+            const int n_items = T::items(p, sc, unit);
+            typename T::Epi e;
+            T::epi_begin(p, sc, unit, rank, row, e);
+            for (int item = 0; item < n_items; ++item, ++it) {
+                const int b = it & 1;
+                const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+                if (!mbar_wait(&sm.acc_full[b], aph, sm.abort_flag, status)) goto epi_done;
+                tc_fence_after();
+                T::template epi_item<kBf16>(p, sc, unit, item, rank, tq + b * 256, e);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (leader)
+                        mbar_arrive(&sm.acc_empty[b]);
+                    else
+                        mbar_arrive_cluster(acc_empty0 + 8u * b);
+                }
+            }
+            T::epi_end(p, sc, rank, e);
+        }
+    epi_done:;
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    // the leader's MMAs write the peer's tensor memory, and the peer's loads
+    // complete on the leader's barriers: nobody leaves before both are done
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
 // ====================================================================== launches
 
 // One named kernel per traits class (the names show up in profiles).
@@ -785,6 +1258,19 @@ GRPO_TC_KERNEL(grpo_dlogits_kernel, DsT)
 GRPO_TC_KERNEL(grpo_dh_kernel, DhT)
 GRPO_TC_KERNEL(grpo_dw_kernel, DwT)
 #undef GRPO_TC_KERNEL
+
+#define GRPO_PAIR_KERNEL(NAME, TRAITS)                                                                         \
+    template <bool kBf16>                                                                                      \
+    __global__ void __launch_bounds__(kThreads, 1)                                                             \
+        NAME(const __grid_constant__ TRAITS::Params p, const __grid_constant__ CUtensorMap mA,                 \
+             const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB) {                \
+        tc_pair_body<TRAITS, kBf16>(p, mA, mA2, mB);                                                           \
+    }
+
+GRPO_PAIR_KERNEL(grpo_fwd_pair_kernel, FwdPairT)
+GRPO_PAIR_KERNEL(grpo_dh_pair_kernel, DhPairT)
+GRPO_PAIR_KERNEL(grpo_dw_pair_kernel, DwPairT)
+#undef GRPO_PAIR_KERNEL
 
 // Persistent launch: one CTA per SM, in clusters of kC; the grid is capped by
 // how many clusters fit on the device at once, so every CTA runs concurrently.
@@ -815,6 +1301,24 @@ static cudaError_t launch_tc(K kern, const typename T::Params& p, const CUtensor
     if (clusters < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(clusters * kC);
     return cudaLaunchKernelEx(&cfg, kern, p, a, a2, b);
+}
+
+cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
+                            const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st) {
+    return bf16 ? launch_tc<FwdPairT, 2>(grpo_fwd_pair_kernel<true>, p, mHp, mHr, mW, n_sm, st)
+                : launch_tc<FwdPairT, 2>(grpo_fwd_pair_kernel<false>, p, mHp, mHr, mW, n_sm, st);
+}
+
+cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm, bool bf16,
+                           cudaStream_t st) {
+    return bf16 ? launch_tc<DhPairT, 2>(grpo_dh_pair_kernel<true>, p, mDS, mDS, mWmn, n_sm, st)
+                : launch_tc<DhPairT, 2>(grpo_dh_pair_kernel<false>, p, mDS, mDS, mWmn, n_sm, st);
+}
+
+cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
+                           bool bf16, cudaStream_t st) {
+    return bf16 ? launch_tc<DwPairT, 2>(grpo_dw_pair_kernel<true>, p, mDSmn, mDSmn, mHcmn, n_sm, st)
+                : launch_tc<DwPairT, 2>(grpo_dw_pair_kernel<false>, p, mDSmn, mDSmn, mHcmn, n_sm, st);
 }
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr, const CUtensorMap& mW,
