@@ -414,7 +414,7 @@ def run_ours(args, ranks):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ranks.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generator; random-init head)",
-        "config": cfg_dict(cfg, {"n_valid": n_valid, "chunk_rows": args.chunk_rows or 8192,
+        "config": cfg_dict(cfg, {"n_valid": n_valid, "chunk_rows": args.chunk_rows or 76 * 128,
                                  "loss_scale": scale[0]}),
         "pct_bf16_peak": {"useful_tflops": useful / t_step / 1e12,
                           "of_burst": useful / t_step / 1e12 / burst,

@@ -70,8 +70,8 @@ typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
  *   beta        : KL coefficient (0.04 in the pages' setting)
  *   eps         : added to the group std in grpo_group_advantages
  *   std_unbiased: 1 -> group std with divisor G-1, 0 -> divisor G
- *   chunk_rows  : masked rows processed per backward chunk (0 -> 8192);
- *                 rounded up to a multiple of 128. */
+ *   chunk_rows  : masked rows processed per backward chunk (0 -> 9728, i.e.
+ *                 76 tiles of 128 rows); rounded up to a multiple of 128. */
 typedef struct {
     int n_groups, G, L, d, V;
     grpo_dtype dtype;

@@ -14,7 +14,10 @@ constexpr int kBK = 64;               // K elements per pipeline stage: one 128-
 constexpr int kBN = 256;              // accumulator columns per MMA tile
 constexpr int kTileSplits = 8;        // vocabulary splits of a forward row tile (forward-only path)
 constexpr int kChunkSplits = 64;      // vocabulary splits of a chunk row tile (forward+backward path)
-constexpr int kDefaultChunkRows = 8192;
+// Default rows per backward chunk: 76 tiles of 128.  On 152 SMs (76 CTA pairs)
+// the chunk's forward units (76 tiles x 64 splits) and its dH units (38 tile
+// pairs x d/256 tiles, for d = 1536, 4096 or 5120) divide evenly over the pairs.
+constexpr int kDefaultChunkRows = 76 * 128;
 constexpr int kMergeThreads = 256;
 constexpr int kIndexThreads = 1024;
 constexpr int kTransformThreads = 256;

@@ -183,12 +183,9 @@ __global__ void __launch_bounds__(kIndexThreads) k_index(const uint8_t* __restri
     }
     if (tid == 0) {
         const int nv = carry_valid;
+        // fixed-size chunks of R_max rows (a multiple of kBM); the last one holds the rest
         const int n_chunks = nv > 0 ? (nv + R_max - 1) / R_max : 0;
-        int rc = 0;
-        if (n_chunks > 0) {
-            rc = (nv + n_chunks - 1) / n_chunks;
-            rc = (rc + kBM - 1) / kBM * kBM;
-        }
+        const int rc = n_chunks > 0 ? R_max : 0;
         counts[C_NVALID] = nv;
         counts[C_NTILES] = carry_tiles;
         counts[C_NCHUNKS] = n_chunks;

@@ -798,7 +798,7 @@ __device__ __forceinline__ void decode_tile_split(int unit, int n_mt, int S, int
 // reference tile of the same 128 compact rows; the leader also keeps the
 // policy exponentials for the backward.
 struct FwdPairT {
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 7;
     static constexpr int kStageBytes = 16384 + 16384;   // A (128x64), B half (128x64)
     using Params = FwdParams;
     struct Sched {
@@ -921,7 +921,7 @@ struct FwdPairT {
 };
 
 struct DhPairT {
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 7;
     static constexpr int kStageBytes = 16384 + 16384;   // A (128 slots x 64 vocab), B half (64 vocab x 128 d)
     using Params = ChunkParams;
     using Sched = ChunkSched;
@@ -1002,7 +1002,7 @@ struct DhPairT {
 };
 
 struct DwPairT {
-    static constexpr int kStages = 6;
+    static constexpr int kStages = 7;
     static constexpr int kStageBytes = 16384 + 16384;   // A (64 slots x 128 vocab), B half (64 slots x 128 d)
     using Params = ChunkParams;
     using Sched = ChunkSched;
