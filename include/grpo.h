@@ -188,7 +188,7 @@ enum {
     GRPO_PROF_MERGE,
     GRPO_PROF_CLEAR,
     GRPO_PROF_GATHER,
-    GRPO_PROF_DS,
+    GRPO_PROF_DLOGITS,
     GRPO_PROF_DH,
     GRPO_PROF_DW,
     GRPO_PROF_KINDS

@@ -22,7 +22,7 @@ __all__ = [
 ]
 
 # kernel kinds of the diagnostics interface, in the order of the GRPO_PROF_* enum
-PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "ds", "dh", "dw")
+PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "dlogits", "dh", "dw")
 
 BF16, FP16 = 0, 1
 

@@ -483,7 +483,7 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
                    [&] { return launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
+        if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
             cudaSuccess)

@@ -21,9 +21,8 @@ constexpr int kDefaultChunkRows = 76 * 128;
 constexpr int kMergeThreads = 256;
 constexpr int kIndexThreads = 1024;
 constexpr int kTransformThreads = 256;
-// CTAs per cluster sharing one B tile through TMA multicast (1, 2 or 4)
+// CTAs per cluster of the forward-only kernel (clusters share each W tile through TMA multicast)
 constexpr int kClusterFwd = 1;
-constexpr int kClusterBwd = 2;
 
 // int32 words at the start of the workspace
 enum CountSlot {
@@ -134,11 +133,5 @@ cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const C
                            bool bf16, cudaStream_t st);
 cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
                            bool bf16, cudaStream_t st);
-cudaError_t launch_ds(const ChunkParams& p, const CUtensorMap& mHc, const CUtensorMap& mW, int n_sm, bool bf16,
-                      cudaStream_t st);
-cudaError_t launch_dh(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm,
-                      bool bf16, cudaStream_t st);
-cudaError_t launch_dw(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
-                      bool bf16, cudaStream_t st);
 
 }  // namespace grpo

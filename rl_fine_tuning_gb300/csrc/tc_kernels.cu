@@ -294,283 +294,6 @@ __device__ __forceinline__ bool chunk_setup(const ChunkParams& p, ChunkSched& sc
     return sc.n_c > 0;
 }
 
-// MN-major B: four 64-wide boxes; the CTA of rank r loads the boxes j = r (mod C)
-__device__ __forceinline__ void load_b_mnmajor(const ChunkSched& sc, const CUtensorMap* mB, uint64_t* bar,
-                                               uint8_t* dst, int n0, int d, int k, int rank) {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if ((j % sc.C) != rank || n0 + 64 * j >= d) continue;
-        if (sc.C == 1)
-            tma_load_2d(mB, bar, dst + 8192 * j, n0 + 64 * j, k * kBK);
-        else
-            tma_load_2d_mc(mB, bar, dst + 8192 * j, n0 + 64 * j, k * kBK, static_cast<uint16_t>((1u << sc.C) - 1u));
-    }
-}
-
-struct DsT {
-    static constexpr int kStages = 4;
-    static constexpr int kStageBytes = 16384 + 32768;   // A (128x64), B (256x64)
-    static constexpr int kAccBufs = 2;
-    static constexpr int kAccStride = 256;
-    using Params = ChunkParams;
-    using Sched = ChunkSched;
-    struct Coord {
-        int m0, n0;
-    };
-    struct Epi {
-        int unused;
-    };
-    // unit = n-tile * n_g + m-group (m-groups fastest: the chunk's rows stay in L2 while W streams)
-    __device__ static bool setup(const Params& p, Sched& sc, int C) {
-        if (!chunk_setup(p, sc, C)) return false;
-        sc.n_nt = (p.V + kBN - 1) / kBN;
-        sc.n_g = (sc.n_mt + C - 1) / C;
-        sc.ks = p.d / kBK;
-        sc.n_units = sc.n_g * sc.n_nt;
-        return true;
-    }
-    __device__ static int mtile(const Sched& sc, int unit, int rank) { return (unit % sc.n_g) * sc.C + rank; }
-    __device__ static int items(const Params&, const Sched&, int) { return 1; }
-    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
-    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
-        return Coord{mtile(sc, unit, rank) * kBM, (unit / sc.n_g) * kBN};
-    }
-    __device__ static uint32_t tx_bytes(const Params&, const Sched&, const Coord&) { return kStageBytes; }
-    __device__ static void load(const Params&, const Sched& sc, const Coord& c, int k, uint8_t* st, uint64_t* bar,
-                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
-        tma_load_2d(mA, bar, st, k * kBK, c.m0);
-        const int rows = kBN / sc.C;
-        if (sc.C == 1)
-            tma_load_2d(mB, bar, st + 16384, k * kBK, c.n0);
-        else
-            tma_load_2d_mc(mB, bar, st + 16384 + rank * rows * 128, k * kBK, c.n0 + rank * rows,
-                           static_cast<uint16_t>((1u << sc.C) - 1u));
-    }
-    template <bool kBf16>
-    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
-        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, false, false);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            umma_f16(acc, desc_kmajor(st + kk * 32), desc_kmajor(st + 16384 + kk * 32), idesc,
-                     (first && kk == 0) ? 0u : 1u);
-    }
-    __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
-    template <bool kBf16>
-    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
-        const int mt = mtile(sc, unit, rank);
-        if (mt >= sc.n_mt) return;                 // phantom tile: nothing to write
-        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
-        const int slot = mt * kBM + row;
-        const int n0 = (unit / sc.n_g) * kBN;
-        const bool valid = slot < sc.n_c;
-        int t = 0, tok = -1;
-        float coef = 0.f, lse2 = 0.f;
-        if (valid) {
-            t = p.rows[sc.c0 + slot];
-            tok = p.tokens[t];
-            coef = p.scale * p.gco[t];
-            lse2 = p.lse[t] * kLog2e;
-        }
-        uint16_t* out = p.dS + static_cast<int64_t>(slot) * p.V_pad;
-        bool bad = false;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-            const int col0 = n0 + c * 32;
-            if (col0 >= p.V) break;
-            float v[32];
-            tmem_ld32(tacc + c * 32, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const float p0 = fast_exp2(fmaf(v[j], kLog2e, -lse2));
-                const float p1 = fast_exp2(fmaf(v[j + 1], kLog2e, -lse2));
-                const float d0 = coef * ((col0 + j == tok ? 1.f : 0.f) - p0);
-                const float d1 = coef * ((col0 + j + 1 == tok ? 1.f : 0.f) - p1);
-                pk[j / 2] = pack2(d0, d1, kBf16);
-            }
-            if (!kBf16) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
-            }
-            if (col0 + 32 <= p.V) {
-                uint4* o4 = reinterpret_cast<uint4*>(out + col0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (col0 + j < p.V) out[col0 + j] = static_cast<uint16_t>((pk[j / 2] >> (16 * (j & 1))) & 0xFFFFu);
-            }
-        }
-        if (bad) atomicOr(p.found_inf, 1);
-    }
-    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
-};
-
-struct DhT {
-    static constexpr int kStages = 4;
-    static constexpr int kStageBytes = 16384 + 32768;   // A (128 slots x 64 vocab), B (64 vocab x 256 d)
-    static constexpr int kAccBufs = 2;
-    static constexpr int kAccStride = 256;
-    using Params = ChunkParams;
-    using Sched = ChunkSched;
-    struct Coord {
-        int m0, n0;
-    };
-    struct Epi {
-        int unused;
-    };
-    // unit = m-group * n_nt + d-tile (d-tiles fastest: a group's dlogits rows are shared in L2)
-    __device__ static bool setup(const Params& p, Sched& sc, int C) {
-        if (!chunk_setup(p, sc, C)) return false;
-        sc.n_nt = (p.d + kBN - 1) / kBN;
-        sc.n_g = (sc.n_mt + C - 1) / C;
-        sc.ks = (p.V + kBK - 1) / kBK;
-        sc.n_units = sc.n_g * sc.n_nt;
-        return true;
-    }
-    __device__ static int mtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * sc.C + rank; }
-    __device__ static int items(const Params&, const Sched&, int) { return 1; }
-    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
-    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
-        return Coord{mtile(sc, unit, rank) * kBM, (unit % sc.n_nt) * kBN};
-    }
-    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
-        return 16384 + 8192 * min(4, (p.d - c.n0) / 64);
-    }
-    __device__ static void load(const Params& p, const Sched& sc, const Coord& c, int k, uint8_t* st, uint64_t* bar,
-                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
-        tma_load_2d(mA, bar, st, k * kBK, c.m0);
-        load_b_mnmajor(sc, mB, bar, st + 16384, c.n0, p.d, k, rank);
-    }
-    template <bool kBf16>
-    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
-        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, false, true);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            umma_f16(acc, desc_kmajor(st + kk * 32), desc_mnmajor(st + 16384 + kk * 2048), idesc,
-                     (first && kk == 0) ? 0u : 1u);
-    }
-    __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
-    template <bool kBf16>
-    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
-        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
-        const int slot = mtile(sc, unit, rank) * kBM + row;
-        const int n0 = (unit % sc.n_nt) * kBN;
-        const bool valid = slot < sc.n_c;
-        if (!__any_sync(0xffffffffu, valid)) return;
-        const int t = valid ? p.rows[sc.c0 + slot] : 0;
-        uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
-        bool bad = false;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-            const int col0 = n0 + c * 32;
-            if (col0 >= p.d) break;
-            float v[32];
-            tmem_ld32(tacc + c * 32, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2(v[j] * sc.winv, v[j + 1] * sc.winv, kBf16);
-            if (!kBf16) {
-#pragma unroll
-                for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
-            }
-            if (valid) {
-                uint4* o4 = reinterpret_cast<uint4*>(out + col0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            }
-        }
-        if (bad && valid) atomicOr(p.found_inf, 1);
-    }
-    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
-};
-
-struct DwT {
-    static constexpr int kStages = 4;
-    static constexpr int kStageBytes = 16384 + 32768;   // A (64 slots x 128 vocab), B (64 slots x 256 d)
-    static constexpr int kAccBufs = 2;
-    static constexpr int kAccStride = 256;
-    using Params = ChunkParams;
-    using Sched = ChunkSched;
-    struct Coord {
-        int v0, n0;
-    };
-    struct Epi {
-        int unused;
-    };
-    // unit = vocab-group * n_nt + d-tile (d-tiles fastest: a group's dlogits columns are shared in L2)
-    __device__ static bool setup(const Params& p, Sched& sc, int C) {
-        if (!chunk_setup(p, sc, C)) return false;
-        sc.n_nt = (p.d + kBN - 1) / kBN;
-        sc.n_g = ((p.V + kBM - 1) / kBM + C - 1) / C;
-        sc.ks = (sc.n_c + kBK - 1) / kBK;
-        sc.n_units = sc.n_g * sc.n_nt;
-        return true;
-    }
-    __device__ static int vtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * sc.C + rank; }
-    __device__ static int items(const Params&, const Sched&, int) { return 1; }
-    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
-    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
-        return Coord{vtile(sc, unit, rank) * kBM, (unit % sc.n_nt) * kBN};
-    }
-    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
-        return 16384 + 8192 * min(4, (p.d - c.n0) / 64);
-    }
-    __device__ static void load(const Params& p, const Sched& sc, const Coord& c, int k, uint8_t* st, uint64_t* bar,
-                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
-        tma_load_2d(mA, bar, st, c.v0, k * kBK);
-        tma_load_2d(mA, bar, st + 8192, c.v0 + 64, k * kBK);
-        load_b_mnmajor(sc, mB, bar, st + 16384, c.n0, p.d, k, rank);
-    }
-    template <bool kBf16>
-    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
-        constexpr uint32_t idesc = make_idesc_f16(128, 256, kBf16, true, true);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-            umma_f16(acc, desc_mnmajor(st + kk * 2048), desc_mnmajor(st + 16384 + kk * 2048), idesc,
-                     (first && kk == 0) ? 0u : 1u);
-    }
-    __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
-    template <bool kBf16>
-    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
-        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
-        const int v = vtile(sc, unit, rank) * kBM + row;
-        const int n0 = (unit % sc.n_nt) * kBN;
-        const bool valid = v < p.V;
-        if (!__any_sync(0xffffffffu, valid)) return;
-        const bool first_chunk = p.chunk == 0;
-        float* out = p.dW + static_cast<int64_t>(valid ? v : 0) * p.d;
-        bool bad = false;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-            const int col0 = n0 + c * 32;
-            if (col0 >= p.d) break;
-            float x[32];
-            tmem_ld32(tacc + c * 32, x);
-            if (valid) {
-                float4* o4 = reinterpret_cast<float4*>(out + col0);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float4 r = make_float4(x[4 * j] * sc.winv, x[4 * j + 1] * sc.winv, x[4 * j + 2] * sc.winv,
-                                           x[4 * j + 3] * sc.winv);
-                    if (!first_chunk) {
-                        const float4 o = o4[j];
-                        r.x += o.x;
-                        r.y += o.y;
-                        r.z += o.z;
-                        r.w += o.w;
-                    }
-                    bad |= !(isfinite(r.x) && isfinite(r.y) && isfinite(r.z) && isfinite(r.w));
-                    o4[j] = r;
-                }
-            }
-        }
-        if (bad) atomicOr(p.found_inf, 1);
-    }
-    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
-};
-
 // ====================================================================== engine
 
 template <class T, bool kBf16, int kC>
@@ -1254,9 +977,6 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
     }
 
 GRPO_TC_KERNEL(grpo_fwd_lse_kernel, FwdT)
-GRPO_TC_KERNEL(grpo_dlogits_kernel, DsT)
-GRPO_TC_KERNEL(grpo_dh_kernel, DhT)
-GRPO_TC_KERNEL(grpo_dw_kernel, DwT)
 #undef GRPO_TC_KERNEL
 
 #define GRPO_PAIR_KERNEL(NAME, TRAITS)                                                                         \
@@ -1325,24 +1045,6 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtenso
                        int n_sm, bool bf16, cudaStream_t st) {
     return bf16 ? launch_tc<FwdT, kClusterFwd>(grpo_fwd_lse_kernel<true, kClusterFwd>, p, mHp, mHr, mW, n_sm, st)
                 : launch_tc<FwdT, kClusterFwd>(grpo_fwd_lse_kernel<false, kClusterFwd>, p, mHp, mHr, mW, n_sm, st);
-}
-
-cudaError_t launch_ds(const ChunkParams& p, const CUtensorMap& mHc, const CUtensorMap& mW, int n_sm, bool bf16,
-                      cudaStream_t st) {
-    return bf16 ? launch_tc<DsT, kClusterBwd>(grpo_dlogits_kernel<true, kClusterBwd>, p, mHc, mHc, mW, n_sm, st)
-                : launch_tc<DsT, kClusterBwd>(grpo_dlogits_kernel<false, kClusterBwd>, p, mHc, mHc, mW, n_sm, st);
-}
-
-cudaError_t launch_dh(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm, bool bf16,
-                      cudaStream_t st) {
-    return bf16 ? launch_tc<DhT, kClusterBwd>(grpo_dh_kernel<true, kClusterBwd>, p, mDS, mDS, mWmn, n_sm, st)
-                : launch_tc<DhT, kClusterBwd>(grpo_dh_kernel<false, kClusterBwd>, p, mDS, mDS, mWmn, n_sm, st);
-}
-
-cudaError_t launch_dw(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm, bool bf16,
-                      cudaStream_t st) {
-    return bf16 ? launch_tc<DwT, kClusterBwd>(grpo_dw_kernel<true, kClusterBwd>, p, mDSmn, mDSmn, mHcmn, n_sm, st)
-                : launch_tc<DwT, kClusterBwd>(grpo_dw_kernel<false, kClusterBwd>, p, mDSmn, mDSmn, mHcmn, n_sm, st);
 }
 
 }  // namespace grpo
