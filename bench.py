@@ -160,7 +160,7 @@ def peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("tc_kernels.cu", "ptx.cuh", "internal.h"):
+    for f in ("tc_kernels.cu", "ptx.cuh"):
         h.update(open(os.path.join(ROOT, "rl_fine_tuning_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
