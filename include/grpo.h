@@ -71,7 +71,20 @@ typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
  *   eps         : added to the group std in grpo_group_advantages
  *   std_unbiased: 1 -> group std with divisor G-1, 0 -> divisor G
  *   chunk_rows  : masked rows processed per backward chunk (0 -> 9728, i.e.
- *                 76 tiles of 128 rows); rounded up to a multiple of 128. */
+ *                 76 tiles of 128 rows); rounded up to a multiple of 128.
+ *   loss_mode   : GRPO_TOKEN_MEAN -- mean of ell_t over all masked rows;
+ *                 GRPO_SEQUENCE_MEAN -- mean over completions (with at least
+ *                 one masked row) of each completion's mean over its rows
+ *   objective   : the per-token objective ("Long-context GRPO", section 4:
+ *                 the four-way experiment; the pages' formula images are
+ *                 lost, so each variant is the reading stated here), with
+ *                 x = p_t - q_t and ell_t = -A + beta * pen_t:
+ *                 GRPO_OBJ_GRPO        detached exp(q - sg(q)) * A, pen = e^x - x - 1
+ *                 GRPO_OBJ_NO_DETACH   same value, but exp(q - q) carries no
+ *                                      gradient: d ell/d q = beta (1 - e^x)
+ *                 GRPO_OBJ_REVERSE_KL_Q  pen = e^q (e^x - x - 1): the penalty
+ *                                      multiplied by the token's policy probability
+ *                 GRPO_OBJ_FORWARD_KL  pen = e^-x + x - 1 */
 typedef struct {
     int n_groups, G, L, d, V;
     grpo_dtype dtype;
@@ -79,9 +92,15 @@ typedef struct {
     float eps;
     int std_unbiased;
     int chunk_rows;
+    int loss_mode;
+    int objective;
 } grpo_shape;
 
-/* Fills a grpo_shape with the pages' defaults (beta 0.04, eps 1e-4, unbiased std). */
+enum { GRPO_TOKEN_MEAN = 0, GRPO_SEQUENCE_MEAN = 1 };
+enum { GRPO_OBJ_GRPO = 0, GRPO_OBJ_NO_DETACH = 1, GRPO_OBJ_REVERSE_KL_Q = 2, GRPO_OBJ_FORWARD_KL = 3 };
+
+/* Fills a grpo_shape with the pages' defaults (beta 0.04, eps 1e-4, unbiased
+ * std, token mean, the GRPO objective). */
 void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, grpo_dtype dtype);
 
 /* Bytes of device workspace grpo_loss_fwd / grpo_loss_fwd_bwd need for this
@@ -118,8 +137,9 @@ int grpo_valid_rows(const uint8_t* mask, const grpo_shape* shape, int32_t* rows_
  *   mask [N] uint8, nonzero = completion token (device, read)
  *   adv [n_groups*G] fp32, one per completion (device, read)
  *   workspace: >= grpo_workspace_bytes(shape) bytes of device memory, 256-byte aligned
- *   loss_out: one fp32 (device) <- mean of ell_t over masked rows (0 if none)
- *   row_stats: NULL or [N x 5] fp32 (device) <- (lse_pol, lse_ref, q, p, kl)
+ *   loss_out: one fp32 (device) <- the mean of ell_t chosen by loss_mode (0 if
+ *             no row is masked in)
+ *   row_stats: NULL or [N x 5] fp32 (device) <- (lse_pol, lse_ref, q, p, pen)
  *              per row; zeros on masked rows
  *   status: one int32 (device) <- 0 or an error code
  * The result is bitwise reproducible from run to run. */

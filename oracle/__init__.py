@@ -10,7 +10,6 @@ sums).  This module only compiles it and marshals numpy arrays.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import subprocess
 
@@ -21,7 +20,9 @@ _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libgrpo_oracle.so")
 
 TYPE_CODE = {"f64": 0, "bf16": 1, "fp16": 2}
-ROW_FIELDS = ("lse_pol", "lse_ref", "zt_pol", "zt_ref", "q", "p", "kl", "ell", "g")
+ROW_FIELDS = ("lse_pol", "lse_ref", "zt_pol", "zt_ref", "q", "p", "pen", "ell", "g")
+OBJECTIVES = {"grpo": 0, "no_detach": 1, "reverse_kl_q": 2, "forward_kl": 3}
+LOSS_MODES = {"token_mean": 0, "sequence_mean": 1}
 
 
 def build(force: bool = False) -> str:
@@ -55,12 +56,15 @@ def _L():
         lib.oracle_valid_rows.argtypes = [p, i64, p]
         lib.oracle_logsumexp.restype = f64
         lib.oracle_logsumexp.argtypes = [p, i32]
-        lib.oracle_row_terms.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, p, i64, p]
+        lib.oracle_row_terms.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, i32, p, i64, p]
+        lib.oracle_row_weights.argtypes = [p, i64, i32, i32, p]
+        lib.oracle_reduce_loss.restype = f64
+        lib.oracle_reduce_loss.argtypes = [p, p, i64, i32, i32]
         lib.oracle_loss.restype = f64
-        lib.oracle_loss.argtypes = [p, p, p, i32, p, p, p, i64, i32, i32, i32, f64, p]
+        lib.oracle_loss.argtypes = [p, p, p, i32, p, p, p, i64, i32, i32, i32, f64, i32, i32, p]
         lib.oracle_surrogate.restype = f64
-        lib.oracle_surrogate.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, p, i64, p, f64]
-        lib.oracle_grad.argtypes = [p, p, i32, p, i32, i32, p, i64, p, p, f64, p, p, i64, p]
+        lib.oracle_surrogate.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, i32, p, i64, p, p]
+        lib.oracle_grad.argtypes = [p, p, i32, p, i32, i32, p, i64, p, p, p, p, p, i64, p]
         _lib = lib
     return _lib
 
@@ -113,7 +117,15 @@ def logsumexp(z):
     return float(_L().oracle_logsumexp(_p(z), z.size))
 
 
-def row_terms(h_pol, h_ref, W, dtype, tokens, adv, L, rows, beta=0.04, W_ref=None):
+def _obj(objective):
+    return OBJECTIVES[objective] if isinstance(objective, str) else int(objective)
+
+
+def _mode(loss_mode):
+    return LOSS_MODES[loss_mode] if isinstance(loss_mode, str) else int(loss_mode)
+
+
+def row_terms(h_pol, h_ref, W, dtype, tokens, adv, L, rows, beta=0.04, W_ref=None, objective=0):
     """Per-row forward terms for the listed rows -> dict of float64 arrays."""
     h_pol, h_ref, W = _mat(h_pol, dtype), _mat(h_ref, dtype), _mat(W, dtype)
     Wr = None if W_ref is None else _mat(W_ref, dtype)
@@ -123,12 +135,26 @@ def row_terms(h_pol, h_ref, W, dtype, tokens, adv, L, rows, beta=0.04, W_ref=Non
     rows = np.ascontiguousarray(rows, np.int32)
     out = np.empty((rows.size, 9), np.float64)
     _L().oracle_row_terms(_p(h_pol), _p(h_ref), _p(W), _p(Wr), TYPE_CODE[dtype], _p(tok), _p(adv),
-                          L, d, V, beta, _p(rows), rows.size, _p(out))
+                          L, d, V, beta, _obj(objective), _p(rows), rows.size, _p(out))
     return {k: out[:, i].copy() for i, k in enumerate(ROW_FIELDS)}
 
 
-def loss(h_pol, h_ref, W, dtype, tokens, mask, adv, L, beta=0.04):
-    """Masked token-mean loss and N_v."""
+def row_weights(rows, L, loss_mode=0):
+    """Loss weight of each listed masked-in row (ascending)."""
+    rows = np.ascontiguousarray(rows, np.int32)
+    out = np.empty(rows.size, np.float64)
+    _L().oracle_row_weights(_p(rows), rows.size, L, _mode(loss_mode), _p(out))
+    return out
+
+
+def reduce_loss(ell, rows, L, loss_mode=0):
+    ell = np.ascontiguousarray(ell, np.float64)
+    rows = np.ascontiguousarray(rows, np.int32)
+    return float(_L().oracle_reduce_loss(_p(ell), _p(rows), rows.size, L, _mode(loss_mode)))
+
+
+def loss(h_pol, h_ref, W, dtype, tokens, mask, adv, L, beta=0.04, objective=0, loss_mode=0):
+    """Loss over the masked rows (token mean or sequence mean) and N_v."""
     h_pol, h_ref, W = _mat(h_pol, dtype), _mat(h_ref, dtype), _mat(W, dtype)
     V, d = W.shape
     tok = np.ascontiguousarray(tokens, np.int32)
@@ -136,14 +162,15 @@ def loss(h_pol, h_ref, W, dtype, tokens, mask, adv, L, beta=0.04):
     adv = np.ascontiguousarray(adv, np.float32)
     nv = ctypes.c_int64(0)
     val = _L().oracle_loss(_p(h_pol), _p(h_ref), _p(W), TYPE_CODE[dtype], _p(tok), _p(mask), _p(adv),
-                           mask.size, L, d, V, beta, ctypes.byref(nv))
+                           mask.size, L, d, V, beta, _obj(objective), _mode(loss_mode), ctypes.byref(nv))
     return float(val), int(nv.value)
 
 
-def surrogate(h_pol, h_ref, W, dtype, tokens, adv, L, rows, c, w, beta=0.04, W_ref=None):
-    """w * sum_i [-A exp(q_i - c_i) + beta KL_i]; c=None re-evaluates c = q (no detach).
+def surrogate(h_pol, h_ref, W, dtype, tokens, adv, L, rows, c, w, beta=0.04, W_ref=None, objective=0):
+    """sum_i w_i [-A exp(q_i - c_i) + beta pen_i]; c=None re-evaluates c = q (no detach).
 
-    W_ref: weight of the frozen reference (None: W itself)."""
+    w: per-row weights (or one scalar for all rows); W_ref: weight of the
+    frozen reference (None: W itself)."""
     h_pol, h_ref, W = _mat(h_pol, dtype), _mat(h_ref, dtype), _mat(W, dtype)
     Wr = None if W_ref is None else _mat(W_ref, dtype)
     V, d = W.shape
@@ -151,29 +178,34 @@ def surrogate(h_pol, h_ref, W, dtype, tokens, adv, L, rows, c, w, beta=0.04, W_r
     adv = np.ascontiguousarray(adv, np.float32)
     rows = np.ascontiguousarray(rows, np.int32)
     cc = None if c is None else np.ascontiguousarray(c, np.float64)
+    ww = np.ascontiguousarray(np.broadcast_to(np.asarray(w, np.float64), (rows.size,)))
     return float(_L().oracle_surrogate(_p(h_pol), _p(h_ref), _p(W), _p(Wr), TYPE_CODE[dtype], _p(tok),
-                                       _p(adv), L, d, V, beta, _p(rows), rows.size, _p(cc), w))
+                                       _p(adv), L, d, V, beta, _obj(objective), _p(rows), rows.size, _p(cc),
+                                       _p(ww)))
 
 
 def grad(h_pol, W, dtype, tokens, rows, lse, g, w, want_dH=True, vrows=None, want_dW=True):
-    """dH for the listed rows ([n_rows, d]) and dW for vocabulary rows vrows (all if None)."""
+    """dH for the listed rows ([n_rows, d]) and dW for vocabulary rows vrows (all if None).
+
+    w: per-row loss weights (or one scalar for all rows)."""
     h_pol, W = _mat(h_pol, dtype), _mat(W, dtype)
     V, d = W.shape
     tok = np.ascontiguousarray(tokens, np.int32)
     rows = np.ascontiguousarray(rows, np.int32)
     lse = np.ascontiguousarray(lse, np.float64)
     g = np.ascontiguousarray(g, np.float64)
+    ww = np.ascontiguousarray(np.broadcast_to(np.asarray(w, np.float64), (rows.size,)))
     dH = np.empty((rows.size, d), np.float64) if want_dH else None
     vr = None if vrows is None else np.ascontiguousarray(vrows, np.int32)
     n_v = V if vr is None else vr.size
     dW = np.empty((n_v, d), np.float64) if want_dW else None
     _L().oracle_grad(_p(h_pol), _p(W), TYPE_CODE[dtype], _p(tok), d, V, _p(rows), rows.size,
-                     _p(lse), _p(g), w, _p(dH), _p(vr), 0 if vr is None else vr.size, _p(dW))
+                     _p(lse), _p(g), _p(ww), _p(dH), _p(vr), 0 if vr is None else vr.size, _p(dW))
     return dH, dW
 
 
 def expected(wl, eval_rows=None, vrows=None, mask=None, want_dH=True, want_dW=True,
-             std_unbiased=True):
+             std_unbiased=True, objective=0, loss_mode=0):
     """Everything the library computes for a synthetic workload, in fp64.
 
     eval_rows: the valid rows whose per-row terms (and dH) are computed; None
@@ -186,14 +218,15 @@ def expected(wl, eval_rows=None, vrows=None, mask=None, want_dH=True, want_dW=Tr
         mask = build_mask(wl.lengths, cfg.L)
     rows_all = valid_rows(mask)
     n_valid = rows_all.size
-    w = 1.0 / max(n_valid, 1)
+    w_all = row_weights(rows_all, cfg.L, loss_mode)
     full = eval_rows is None
     rows = rows_all if full else np.ascontiguousarray(eval_rows, np.int32)
-    terms = row_terms(wl.h_pol, wl.h_ref, wl.W, cfg.dtype, wl.tokens, adv, cfg.L, rows, cfg.beta)
+    w = w_all if full else w_all[np.searchsorted(rows_all, rows)]
+    terms = row_terms(wl.h_pol, wl.h_ref, wl.W, cfg.dtype, wl.tokens, adv, cfg.L, rows, cfg.beta,
+                      objective=objective)
     out = dict(adv=adv, mask=mask, rows=rows_all, n_valid=n_valid, w=w, eval_rows=rows, terms=terms)
     if full:
-        # exactly rounded sum of the per-row terms, then the token mean
-        out["loss"] = math.fsum(terms["ell"].tolist()) / n_valid if n_valid else 0.0
+        out["loss"] = reduce_loss(terms["ell"], rows_all, cfg.L, loss_mode)
     if want_dH or want_dW:
         dH, dW = grad(wl.h_pol, wl.W, cfg.dtype, wl.tokens, rows, terms["lse_pol"], terms["g"], w,
                       want_dH=want_dH, vrows=vrows, want_dW=want_dW and full)

@@ -24,6 +24,9 @@
  *     extra Q factor (same section).  KL is evaluated as expm1(x) - x.
  *   - Mean over completion tokens (mask), gradient to the hidden states and
  *     to the lm_head weight.
+ *   - The variants of the four-way experiment of the same section and a
+ *     per-completion mean; the pages give no formulas for these (their
+ *     images are lost), so they follow the readings stated at each function.
  *
  * Everything is fp64 on inputs widened exactly from their storage type
  * (bf16 / fp16 / double).  Sums run in ascending index order.  OpenMP only
@@ -165,14 +168,51 @@ double oracle_logsumexp(const double* z, int V) {
 
 /* ---- per-row forward terms ----------------------------------------------- */
 
+/* Objectives of the four-way experiment ("Long-context GRPO", section 4), with
+ * x = p - q (reference minus policy log-prob of the sampled token):
+ *   0  GRPO as implemented: detached factor exp(q - sg q) * A and the
+ *      reverse-KL estimator pen = exp(x) - x - 1
+ *   1  the same without the detach: exp(q - q) is the constant 1, so the
+ *      policy-gradient term carries no gradient
+ *   2  the reverse-KL term multiplied by Q, the policy probability of the
+ *      token: pen = exp(q) (exp(x) - x - 1)
+ *   3  forward KL instead: pen = exp(-x) + x - 1
+ * The per-token objective is ell = -A + beta * pen (the policy-gradient
+ * factor has value 1 in every variant) and g = d ell / d q of the surrogate
+ * in which sg(q) is a constant. */
+static void objective_terms(int objective, double A, double q, double p, double beta, double* pen,
+                            double* ell, double* g) {
+    double x = p - q;
+    double k_rev = expm1(x) - x;                  /* exp(x) - x - 1 without cancellation */
+    switch (objective) {
+        case 1:
+            *pen = k_rev;
+            *g = -beta * expm1(x);                /* d/dq beta (e^x - x - 1) */
+            break;
+        case 2:
+            *pen = exp(q) * k_rev;
+            *g = -A - beta * x * exp(q);          /* d/dq e^q (e^x - x - 1) = -x e^q */
+            break;
+        case 3:
+            *pen = expm1(-x) + x;                 /* exp(q-p) - (q-p) - 1 */
+            *g = -A + beta * expm1(-x);           /* d/dq: e^(q-p) - 1 */
+            break;
+        default:
+            *pen = k_rev;
+            *g = -A - beta * expm1(x);            /* -A + beta (1 - e^x) */
+            break;
+    }
+    *ell = -A + beta * *pen;
+}
+
 /* out[i*9 + .] for row t = rows[i]:
- *   0 lse_pol  1 lse_ref  2 z_pol[tok]  3 z_ref[tok]  4 q  5 p  6 kl  7 ell  8 g
+ *   0 lse_pol  1 lse_ref  2 z_pol[tok]  3 z_ref[tok]  4 q  5 p  6 pen  7 ell  8 g
  * adv is per sequence; row t belongs to sequence t / L.
  * The reference logits use W_ref (NULL: the same W).  The frozen reference
  * is a constant of the objective: no gradient is taken through it. */
 void oracle_row_terms(const void* h_pol, const void* h_ref, const void* W, const void* W_ref,
                       int type, const int32_t* tokens, const float* adv, int L, int d, int V,
-                      double beta, const int32_t* rows, int64_t n_rows, double* out) {
+                      double beta, int objective, const int32_t* rows, int64_t n_rows, double* out) {
     if (!W_ref) W_ref = W;
 #pragma omp parallel
     {
@@ -191,65 +231,117 @@ void oracle_row_terms(const void* h_pol, const void* h_ref, const void* W, const
             double zt_ref = z[tok];
             double q = zt_pol - lse_pol;
             double p = zt_ref - lse_ref;
-            double x = p - q;
-            double kl = expm1(x) - x;                 /* exp(x) - x - 1 */
-            double ell = -A + beta * kl;              /* value of -[exp(q-sg q) A - beta KL] */
-            double g = -A - beta * expm1(x);          /* d ell / d q = -A + beta (1 - e^x) */
+            double pen, ell, g;
+            objective_terms(objective, A, q, p, beta, &pen, &ell, &g);
             double* o = out + (size_t)i * 9;
             o[0] = lse_pol; o[1] = lse_ref; o[2] = zt_pol; o[3] = zt_ref;
-            o[4] = q; o[5] = p; o[6] = kl; o[7] = ell; o[8] = g;
+            o[4] = q; o[5] = p; o[6] = pen; o[7] = ell; o[8] = g;
         }
         free(hrow);
         free(z);
     }
 }
 
-/* loss = sum over masked rows of ell / max(N_v, 1); also returns N_v */
+/* ---- the mean over completion tokens -------------------------------------- */
+
+/* Per-row weight of the loss for the listed (masked-in, ascending) rows:
+ *   loss_mode 0: 1 / N_v                       (mean over all completion tokens)
+ *   loss_mode 1: 1 / (n_active * len_i)        (mean over completions of the
+ *                token mean of each; len_i = masked-in rows of completion i,
+ *                n_active = completions with len_i > 0) */
+void oracle_row_weights(const int32_t* rows, int64_t n_rows, int L, int loss_mode, double* w) {
+    if (loss_mode == 1) {
+        int64_t i = 0, n_active = 0;
+        while (i < n_rows) {                      /* rows are ascending: completions are contiguous runs */
+            int64_t seq = rows[i] / L, j = i;
+            while (j < n_rows && rows[j] / L == seq) ++j;
+            ++n_active;
+            i = j;
+        }
+        i = 0;
+        while (i < n_rows) {
+            int64_t seq = rows[i] / L, j = i;
+            while (j < n_rows && rows[j] / L == seq) ++j;
+            for (int64_t k = i; k < j; ++k) w[k] = 1.0 / ((double)n_active * (double)(j - i));
+            i = j;
+        }
+    } else {
+        for (int64_t i = 0; i < n_rows; ++i) w[i] = 1.0 / (double)n_rows;
+    }
+}
+
+/* The loss from per-row objectives of all masked-in rows (ascending):
+ * token mean, or the mean over completions of each completion's token mean. */
+double oracle_reduce_loss(const double* ell, const int32_t* rows, int64_t n_rows, int L, int loss_mode) {
+    if (n_rows == 0) return 0.0;
+    if (loss_mode != 1) {
+        double s = 0.0;
+        for (int64_t i = 0; i < n_rows; ++i) s = s + ell[i];
+        return s / (double)n_rows;
+    }
+    double total = 0.0;
+    int64_t n_active = 0, i = 0;
+    while (i < n_rows) {
+        int64_t seq = rows[i] / L, j = i;
+        double s = 0.0;
+        while (j < n_rows && rows[j] / L == seq) s = s + ell[j++];
+        total = total + s / (double)(j - i);
+        ++n_active;
+        i = j;
+    }
+    return total / (double)n_active;
+}
+
+/* loss over the masked rows for an objective and a mean; also returns N_v */
 double oracle_loss(const void* h_pol, const void* h_ref, const void* W, int type,
                    const int32_t* tokens, const uint8_t* mask, const float* adv,
-                   int64_t N, int L, int d, int V, double beta, int64_t* n_valid_out) {
+                   int64_t N, int L, int d, int V, double beta, int objective, int loss_mode,
+                   int64_t* n_valid_out) {
     int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N > 0 ? N : 1));
     int64_t nv = oracle_valid_rows(mask, N, rows);
     double* terms = (double*)malloc(sizeof(double) * 9 * (size_t)(nv > 0 ? nv : 1));
-    oracle_row_terms(h_pol, h_ref, W, NULL, type, tokens, adv, L, d, V, beta, rows, nv, terms);
-    double s = 0.0;
-    for (int64_t i = 0; i < nv; ++i) s = s + terms[(size_t)i * 9 + 7];
+    double* ell = (double*)malloc(sizeof(double) * (size_t)(nv > 0 ? nv : 1));
+    oracle_row_terms(h_pol, h_ref, W, NULL, type, tokens, adv, L, d, V, beta, objective, rows, nv, terms);
+    for (int64_t i = 0; i < nv; ++i) ell[i] = terms[(size_t)i * 9 + 7];
+    double loss = oracle_reduce_loss(ell, rows, nv, L, loss_mode);
+    free(ell);
     free(terms);
     free(rows);
     if (n_valid_out) *n_valid_out = nv;
-    return nv > 0 ? s / (double)nv : 0.0;
+    return loss;
 }
 
-/* Surrogate objective whose gradient is the GRPO gradient:
- *   J = w * sum_i [ -A exp(q_i - c_i) + beta (exp(p_i-q_i) - (p_i-q_i) - 1) ]
+/* Surrogate objective whose gradient is the gradient of the chosen objective:
+ *   J = sum_i w_i [ -A exp(q_i - c_i) + beta pen_i ]
  * With c held at q's value this is the detached objective; passing
  * c == NULL re-evaluates c = q inside, i.e. the variant without the detach. */
 double oracle_surrogate(const void* h_pol, const void* h_ref, const void* W, const void* W_ref,
                         int type, const int32_t* tokens, const float* adv, int L, int d, int V,
-                        double beta, const int32_t* rows, int64_t n_rows, const double* c, double w) {
+                        double beta, int objective, const int32_t* rows, int64_t n_rows, const double* c,
+                        const double* w) {
     double* terms = (double*)malloc(sizeof(double) * 9 * (size_t)(n_rows > 0 ? n_rows : 1));
-    oracle_row_terms(h_pol, h_ref, W, W_ref, type, tokens, adv, L, d, V, beta, rows, n_rows, terms);
+    oracle_row_terms(h_pol, h_ref, W, W_ref, type, tokens, adv, L, d, V, beta, objective, rows, n_rows, terms);
     double s = 0.0;
     for (int64_t i = 0; i < n_rows; ++i) {
         const double* o = terms + (size_t)i * 9;
         double A = (double)adv[rows[i] / L];
         double ci = c ? c[i] : o[4];
-        s = s + (-A * exp(o[4] - ci) + beta * o[6]);
+        s = s + w[i] * (-A * exp(o[4] - ci) + beta * o[6]);
     }
     free(terms);
-    return w * s;
+    return s;
 }
 
 /* ---- backward ------------------------------------------------------------ */
 
-/* dS[t,v] = w * g_t * (1[v == tok_t] - exp(z_tv - lse_t)) for the policy logits.
+/* dS[t,v] = w_t * g_t * (1[v == tok_t] - exp(z_tv - lse_t)) for the policy logits.
  *   dH[i,:] = sum_v dS[rows[i], v] * W[v,:]                 (if dH != NULL)
  *   dW[j,:] = sum_i dS[rows[i], vrows[j]] * h_pol[rows[i],:] (if dW != NULL;
  *             vrows == NULL means all V vocabulary rows in order)
- * lse and g are per listed row (from oracle_row_terms). */
+ * lse, g and the loss weights w are per listed row. */
 void oracle_grad(const void* h_pol, const void* W, int type, const int32_t* tokens,
                  int d, int V, const int32_t* rows, int64_t n_rows,
-                 const double* lse, const double* g, double w,
+                 const double* lse, const double* g, const double* w,
                  double* dH, const int32_t* vrows, int64_t n_vrows, double* dW) {
     if (dH) {
 #pragma omp parallel
@@ -265,7 +357,7 @@ void oracle_grad(const void* h_pol, const void* W, int type, const int32_t* toke
                 row_logits(h_pol, W, type, t, d, V, z, hrow);
                 for (int k = 0; k < d; ++k) out[k] = 0.0;
                 for (int v = 0; v < V; ++v) {
-                    double dS = w * g[i] * ((v == tok ? 1.0 : 0.0) - exp(z[v] - lse[i]));
+                    double dS = w[i] * g[i] * ((v == tok ? 1.0 : 0.0) - exp(z[v] - lse[i]));
                     load_row(W, type, v, d, wrow);
                     for (int k = 0; k < d; ++k) out[k] = out[k] + dS * wrow[k];
                 }
@@ -289,7 +381,7 @@ void oracle_grad(const void* h_pol, const void* W, int type, const int32_t* toke
                     int64_t t = rows[i];
                     load_row(h_pol, type, t, d, hrow);
                     double z = dot_w(hrow, W, type, v, d);
-                    double dS = w * g[i] * ((v == tokens[t] ? 1.0 : 0.0) - exp(z - lse[i]));
+                    double dS = w[i] * g[i] * ((v == tokens[t] ? 1.0 : 0.0) - exp(z - lse[i]));
                     for (int k = 0; k < d; ++k) out[k] = out[k] + dS * hrow[k];
                 }
             }

@@ -25,6 +25,8 @@ __all__ = [
 PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "dlogits", "dh", "dw")
 
 BF16, FP16 = 0, 1
+TOKEN_MEAN, SEQUENCE_MEAN = 0, 1
+OBJECTIVES = {"grpo": 0, "no_detach": 1, "reverse_kl_q": 2, "forward_kl": 3}
 
 
 class GrpoError(RuntimeError):
@@ -38,7 +40,8 @@ class GrpoShape(ctypes.Structure):
     _fields_ = [
         ("n_groups", ctypes.c_int), ("G", ctypes.c_int), ("L", ctypes.c_int), ("d", ctypes.c_int),
         ("V", ctypes.c_int), ("dtype", ctypes.c_int), ("beta", ctypes.c_float), ("eps", ctypes.c_float),
-        ("std_unbiased", ctypes.c_int), ("chunk_rows", ctypes.c_int),
+        ("std_unbiased", ctypes.c_int), ("chunk_rows", ctypes.c_int), ("loss_mode", ctypes.c_int),
+        ("objective", ctypes.c_int),
     ]
 
     @property
@@ -124,10 +127,13 @@ def _check(code: int, what: str):
         raise GrpoError(code, what)
 
 
-def make_shape(n_groups, G, L, d, V, dtype=BF16, beta=0.04, eps=1e-4, std_unbiased=True, chunk_rows=0):
+def make_shape(n_groups, G, L, d, V, dtype=BF16, beta=0.04, eps=1e-4, std_unbiased=True, chunk_rows=0,
+               loss_mode=TOKEN_MEAN, objective=0):
     s = GrpoShape()
     load().grpo_shape_init(ctypes.byref(s), n_groups, G, L, d, V, dtype)
     s.beta, s.eps, s.std_unbiased, s.chunk_rows = beta, eps, int(bool(std_unbiased)), chunk_rows
+    s.loss_mode = int(loss_mode)
+    s.objective = OBJECTIVES[objective] if isinstance(objective, str) else int(objective)
     return s
 
 

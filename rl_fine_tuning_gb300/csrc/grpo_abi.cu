@@ -68,6 +68,8 @@ bool shape_ok(const grpo_shape& s) {
     const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
     if (N > (1LL << 31) - (1LL << 16)) return false;
     if (s.chunk_rows < 0) return false;
+    if (s.loss_mode != GRPO_TOKEN_MEAN && s.loss_mode != GRPO_SEQUENCE_MEAN) return false;
+    if (s.objective < GRPO_OBJ_GRPO || s.objective > GRPO_OBJ_FORWARD_KL) return false;
     return true;
 }
 
@@ -159,6 +161,7 @@ bool ws_layout(const grpo_shape& s, WsLayout* o) {
     o->nc32 = (s.V + 31) / 32;
     o->nblk = static_cast<int>((N + kMergeThreads - 1) / kMergeThreads);
     o->n_sched = static_cast<int>(2 + (N + o->R - 1) / o->R);
+    o->n_seq = s.n_groups * s.G;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -168,6 +171,7 @@ bool ws_layout(const grpo_shape& s, WsLayout* o) {
     // forward-only path (also what the workspace-free forward uses): everything below `hc`
     o->counts = take(C_COUNT_WORDS * 4);
     o->sched = take(static_cast<size_t>(o->n_sched) * 4);
+    o->seqcnt = take(static_cast<size_t>(o->n_seq) * 4);
     o->tiles = take(static_cast<size_t>(N) * 8);
     o->rows = take(static_cast<size_t>(N) * 4);
     o->part = take(static_cast<size_t>(N) * o->S * 16);
@@ -237,6 +241,9 @@ MergeParams merge_params(const Inputs& in, const WsLayout& L, char* w, int chunk
     mp.L = s.L;
     mp.V = s.V;
     mp.beta = s.beta;
+    mp.loss_mode = s.loss_mode;
+    mp.objective = s.objective;
+    mp.seqcnt = reinterpret_cast<const int*>(w + L.seqcnt);
     mp.N = L.N;
     mp.lse = reinterpret_cast<float*>(w + L.lse);
     mp.gco = reinterpret_cast<float*>(w + L.gco);
@@ -264,13 +271,19 @@ FwdParams fwd_params(const Inputs& in, const WsLayout& L, char* w) {
 }
 
 int run_index(const Inputs& in, const WsLayout& L, char* w, cudaStream_t st) {
-    return launch(GRPO_PROF_INDEX, st, [&] {
-               return launch_index(in.mask, L.N, L.R, reinterpret_cast<int*>(w + L.counts),
-                                   reinterpret_cast<int*>(w + L.rows), reinterpret_cast<int2*>(w + L.tiles),
-                                   reinterpret_cast<int*>(w + L.sched), L.n_sched, in.status, st);
-           }) == cudaSuccess
-               ? GRPO_OK
-               : GRPO_ERR_LAUNCH;
+    if (launch(GRPO_PROF_INDEX, st, [&] {
+            return launch_index(in.mask, L.N, L.R, reinterpret_cast<int*>(w + L.counts),
+                                reinterpret_cast<int*>(w + L.rows), reinterpret_cast<int2*>(w + L.tiles),
+                                reinterpret_cast<int*>(w + L.sched), L.n_sched, in.status, st);
+        }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (in.shape->loss_mode == GRPO_SEQUENCE_MEAN &&
+        launch(GRPO_PROF_INDEX, st, [&] {
+            return launch_seq_counts(in.mask, L.n_seq, in.shape->L, reinterpret_cast<int*>(w + L.seqcnt),
+                                     reinterpret_cast<int*>(w + L.counts), st);
+        }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    return GRPO_OK;
 }
 
 int run_loss_reduce(const Inputs& in, const WsLayout& L, char* w, cudaStream_t st) {
@@ -328,6 +341,8 @@ void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, gr
     s->eps = 1e-4f;
     s->std_unbiased = 1;
     s->chunk_rows = 0;
+    s->loss_mode = GRPO_TOKEN_MEAN;
+    s->objective = GRPO_OBJ_GRPO;
 }
 
 size_t grpo_workspace_bytes(const grpo_shape* shape) {

@@ -31,11 +31,12 @@ enum CountSlot {
     C_NCHUNKS = 2,     // backward chunks
     C_CHUNK_ROWS = 3,  // rows per backward chunk (multiple of 128)
     C_WINV = 4,        // 1 / max(N_valid, 1) as float bits
+    C_NACT = 5,        // completions with at least one masked-in row
     C_COUNT_WORDS = 16
 };
 
 struct WsLayout {
-    size_t counts, sched, tiles, rows, part, zt, lse, gco, ell, blocksum, hc, hcr, partc, mx, ds, total;
+    size_t counts, sched, seqcnt, tiles, rows, part, zt, lse, gco, ell, blocksum, hc, hcr, partc, mx, ds, total;
     int S, nps;      // forward-only path: vocabulary splits, N-tiles per split (partials by row)
     int Sc, npsc;    // chunked path: vocabulary splits, N-tiles per split (partials by chunk slot)
     int n_ntiles;    // ceil(V / kBN)
@@ -44,6 +45,7 @@ struct WsLayout {
     int nc32;        // 32-column groups per vocabulary row
     int nblk;        // loss-reduction blocks
     int n_sched;     // scheduler counters
+    int n_seq;       // completions (n_groups * G)
     int64_t N;
 };
 
@@ -100,6 +102,9 @@ struct MergeParams {
     int R;                  // chunk rows (buffer height)
     int S, L, V;
     float beta;
+    int loss_mode;          // GRPO_TOKEN_MEAN / GRPO_SEQUENCE_MEAN
+    int objective;          // GRPO_OBJ_*
+    const int* seqcnt;      // masked-in rows per completion
     int64_t N;
     float* lse;
     float* gco;
@@ -115,6 +120,7 @@ cudaError_t launch_advantages(const float* r, int n_groups, int G, float eps, in
                               cudaStream_t st);
 cudaError_t launch_build_mask(const int32_t* lengths, int n_seq, int L, uint8_t* mask, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+cudaError_t launch_seq_counts(const uint8_t* mask, int n_seq, int L, int* seqcnt, int* counts, cudaStream_t st);
 cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, cudaStream_t st);
 cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, int nblk, const int* counts,
                                float* loss_out, cudaStream_t st);

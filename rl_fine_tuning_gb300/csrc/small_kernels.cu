@@ -191,6 +191,7 @@ __global__ void __launch_bounds__(kIndexThreads) k_index(const uint8_t* __restri
         counts[C_NCHUNKS] = n_chunks;
         counts[C_CHUNK_ROWS] = rc;
         counts[C_WINV] = __float_as_int(1.0f / static_cast<float>(nv > 0 ? nv : 1));
+        counts[C_NACT] = 0;   // counted by k_seq_counts
     }
 }
 
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
         t = p.rows[c0 + slot];
         pidx = slot;
     }
-    float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, kl = 0.f, g = 0.f, ell = 0.f;
+    float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, pen = 0.f, g = 0.f, ell = 0.f;
     if (p.mask[t]) {
         const int tok = p.tokens[t];
         if (tok < 0 || tok >= p.V) {
@@ -266,11 +267,46 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
             q = z.x - lse_p;
             p_ = z.y - lse_r;
             const float x = p_ - q;
-            const float em1 = expm1f(x);
-            kl = em1 - x;
             const float A = p.adv[t / p.L];
-            ell = -A + p.beta * kl;
-            g = -A - p.beta * em1;
+            // penalty and d ell / d q of the chosen objective (x = p - q)
+            switch (p.objective) {
+                case GRPO_OBJ_NO_DETACH: {
+                    const float em1 = expm1f(x);
+                    pen = em1 - x;
+                    g = -p.beta * em1;   // exp(q - q) is constant: no policy-gradient term
+                    break;
+                }
+                case GRPO_OBJ_REVERSE_KL_Q: {
+                    const float eq = expf(q);
+                    pen = eq * (expm1f(x) - x);
+                    g = -A - p.beta * x * eq;
+                    break;
+                }
+                case GRPO_OBJ_FORWARD_KL: {
+                    const float em1n = expm1f(-x);
+                    pen = em1n + x;
+                    g = -A + p.beta * em1n;
+                    break;
+                }
+                default: {
+                    const float em1 = expm1f(x);
+                    pen = em1 - x;
+                    g = -A - p.beta * em1;
+                    break;
+                }
+            }
+            ell = -A + p.beta * pen;
+            if (p.loss_mode == GRPO_SEQUENCE_MEAN) {
+                // weight N_v / (n_active * len_i): the final division by N_v
+                // then yields the mean over completions of their token means
+                const int nv = p.counts[C_NVALID];
+                const int nact = p.counts[C_NACT];
+                const int len = p.seqcnt[t / p.L];
+                const float rel = static_cast<float>(static_cast<double>(nv) /
+                                                     (static_cast<double>(nact) * static_cast<double>(len)));
+                ell *= rel;
+                g *= rel;
+            }
         }
     }
     p.lse[t] = lse_p;
@@ -282,7 +318,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
         o[1] = lse_r;
         o[2] = q;
         o[3] = p_;
-        o[4] = kl;
+        o[4] = pen;
     }
 }
 
@@ -291,6 +327,35 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
     int64_t blocks = (n + kMergeThreads - 1) / kMergeThreads;
     if (blocks < 1) blocks = 1;
     k_merge<<<static_cast<unsigned>(blocks), kMergeThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// masked-in rows per completion; completions with any count toward C_NACT
+__global__ void k_seq_counts(const uint8_t* __restrict__ mask, int n_seq, int L, int* __restrict__ seqcnt,
+                             int* __restrict__ counts) {
+    __shared__ int sh[256];
+    for (int i = blockIdx.x; i < n_seq; i += gridDim.x) {
+        const uint8_t* m = mask + static_cast<int64_t>(i) * L;
+        int c = 0;
+        for (int j = threadIdx.x; j < L; j += 256) c += m[j] != 0;
+        sh[threadIdx.x] = c;
+        __syncthreads();
+        for (int s = 128; s > 0; s >>= 1) {
+            if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+            seqcnt[i] = sh[0];
+            if (sh[0] > 0) atomicAdd(counts + C_NACT, 1);
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_seq_counts(const uint8_t* mask, int n_seq, int L, int* seqcnt, int* counts, cudaStream_t st) {
+    int blocks = n_seq < 4096 ? n_seq : 4096;
+    if (blocks < 1) blocks = 1;
+    k_seq_counts<<<blocks, 256, 0, st>>>(mask, n_seq, L, seqcnt, counts);
     return cudaGetLastError();
 }
 

@@ -28,17 +28,18 @@ def host_f64(x, dtype: str) -> np.ndarray:
     return synth.bits_to_f32(b, dtype).astype(np.float64)
 
 
-def shape_for(cfg, chunk_rows=0, beta=None):
+def shape_for(cfg, chunk_rows=0, beta=None, objective=0, loss_mode=0, std_unbiased=True):
     return rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.BF16 if cfg.dtype == "bf16" else rg.FP16,
-                         beta=cfg.beta if beta is None else beta, eps=cfg.eps, chunk_rows=chunk_rows)
+                         beta=cfg.beta if beta is None else beta, eps=cfg.eps, chunk_rows=chunk_rows,
+                         objective=objective, loss_mode=loss_mode, std_unbiased=std_unbiased)
 
 
 class DeviceWorkload:
-    def __init__(self, wl, mask=None, chunk_rows=0):
+    def __init__(self, wl, mask=None, chunk_rows=0, objective=0, loss_mode=0, std_unbiased=True):
         t = torch()
         cfg = wl.cfg
         self.cfg = cfg
-        self.shape = shape_for(cfg, chunk_rows)
+        self.shape = shape_for(cfg, chunk_rows, objective=objective, loss_mode=loss_mode, std_unbiased=std_unbiased)
         self.h_pol = dev_bits(wl.h_pol, cfg.dtype)
         self.h_ref = dev_bits(wl.h_ref, cfg.dtype)
         self.W = dev_bits(wl.W, cfg.dtype)
@@ -46,7 +47,7 @@ class DeviceWorkload:
         self.lengths = t.from_numpy(wl.lengths).cuda()
         self.rewards = t.from_numpy(wl.rewards).cuda()
         self.adv = t.empty(cfg.n_seq, dtype=t.float32, device="cuda")
-        rg.grpo_group_advantages(self.rewards, cfg.n_groups, cfg.G, cfg.eps, True, self.adv)
+        rg.grpo_group_advantages(self.rewards, cfg.n_groups, cfg.G, cfg.eps, std_unbiased, self.adv)
         if mask is None:
             self.mask = t.empty(cfg.N, dtype=t.uint8, device="cuda")
             rg.grpo_build_mask(self.lengths, self.shape, self.mask)

@@ -41,12 +41,13 @@ def test_shape_struct_layout_matches_binding(tmp_path):
     prog = tmp_path / "sz.c"
     prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "grpo.h"\n'
                     'int main(void){printf("%zu", sizeof(grpo_shape));'
-                    'const char* n[]={"n_groups","G","L","d","V","dtype","beta","eps","std_unbiased","chunk_rows"};'
+                    'const char* n[]={"n_groups","G","L","d","V","dtype","beta","eps","std_unbiased","chunk_rows",'
+                    '"loss_mode","objective"};'
                     'size_t o[]={offsetof(grpo_shape,n_groups),offsetof(grpo_shape,G),offsetof(grpo_shape,L),'
                     'offsetof(grpo_shape,d),offsetof(grpo_shape,V),offsetof(grpo_shape,dtype),'
                     'offsetof(grpo_shape,beta),offsetof(grpo_shape,eps),offsetof(grpo_shape,std_unbiased),'
-                    'offsetof(grpo_shape,chunk_rows)};'
-                    'for(int i=0;i<10;i++)printf(" %s=%zu",n[i],o[i]);return 0;}\n')
+                    'offsetof(grpo_shape,chunk_rows),offsetof(grpo_shape,loss_mode),offsetof(grpo_shape,objective)};'
+                    'for(int i=0;i<12;i++)printf(" %s=%zu",n[i],o[i]);return 0;}\n')
     exe = tmp_path / "sz"
     subprocess.check_call(["gcc", "-I" + os.path.join(ROOT, "include"), str(prog), "-o", str(exe)])
     out = subprocess.check_output([str(exe)], text=True).split()
@@ -92,6 +93,10 @@ def test_validation_codes_without_a_device(lib):
     assert f(*args[:6], ctypes.byref(bad), *args[7:]) == 2               # d not a multiple of 64
     bad.dtype = 7
     assert f(*args[:6], ctypes.byref(bad), *args[7:]) == 5               # unknown dtype
+    for field, val in (("loss_mode", 2), ("objective", 4), ("objective", -1)):
+        b2 = rg.make_shape(1, 4, 64, 128, 1024)
+        setattr(b2, field, val)
+        assert f(*args[:6], ctypes.byref(b2), *args[7:]) == 2, field     # unknown mode / objective
     assert lib.grpo_group_advantages(P, 0, 4, ctypes.c_float(1e-4), 1, P, None) == 2
     assert lib.grpo_group_advantages(None, 1, 4, ctypes.c_float(1e-4), 1, P, None) == 1
     fb = lib.grpo_loss_fwd_bwd

@@ -122,7 +122,7 @@ def test_full_mask_sampled_rows(big):
     for col, key in ((0, "lse_pol"), (1, "lse_ref"), (2, "q"), (3, "p")):
         ref = exp["terms"][key]
         assert np.all(np.abs(rs[:, col] - ref) <= 1e-3 * np.maximum(1.0, np.abs(ref))), key
-    assert np.all(np.abs(rs[:, 4] - exp["terms"]["kl"]) <= 1e-5 + 1e-2 * np.abs(exp["terms"]["kl"]))
+    assert np.all(np.abs(rs[:, 4] - exp["terms"]["pen"]) <= 1e-5 + 1e-2 * np.abs(exp["terms"]["pen"]))
     dH = res["dH_rows"] / scale
     assert np.abs(dH - exp["dH"]).max() <= 2e-2 * np.abs(exp["dH"]).max()
     # the loss is the token mean of the per-row objective; its advantage part is exact
@@ -130,7 +130,7 @@ def test_full_mask_sampled_rows(big):
     ell = -A + cfg.beta * res["row_stats"][rows, 4]
     assert abs(res["loss"] - ell.mean()) <= 1e-5 * max(1e-3, abs(ell.mean()))
     a_part = -float(np.sum(big.lengths * exp["adv"].astype(np.float64))) / rows.size
-    kl_ref_mean = float(np.mean(exp["terms"]["kl"]))
+    kl_ref_mean = float(np.mean(exp["terms"]["pen"]))
     assert res["loss"] - a_part >= 0
     # the KL part of the loss is beta times a mean KL of the size the sampled rows show
     kl_gpu_mean = (res["loss"] - a_part) / cfg.beta

@@ -34,8 +34,8 @@ def assert_fwd_parity(res, exp):
         err = np.abs(rs[:, col] - ref)
         lim = STAT_TOL * np.maximum(1.0, np.abs(ref))
         assert np.all(err <= lim), (key, float(err.max()), int(np.argmax(err - lim)))
-    kerr = np.abs(rs[:, 4] - exp["terms"]["kl"])
-    assert np.all(kerr <= 1e-5 + 1e-2 * np.abs(exp["terms"]["kl"])), float(kerr.max())
+    kerr = np.abs(rs[:, 4] - exp["terms"]["pen"])
+    assert np.all(kerr <= 1e-5 + 1e-2 * np.abs(exp["terms"]["pen"])), float(kerr.max())
     masked = np.flatnonzero(exp["mask"] == 0)
     assert np.all(res["row_stats"][masked] == 0)
 
@@ -106,13 +106,16 @@ def test_mask_and_valid_rows_bit_exact(case):
 
 # ------------------------------------------------------------------ fused loss
 
-def _run(cfg, seed=0, mask=None, chunk_rows=0, loss_scale=1.0, fwd_only=False, eval_rows=None, vrows=None):
+def _run(cfg, seed=0, mask=None, chunk_rows=0, loss_scale=1.0, fwd_only=False, eval_rows=None, vrows=None,
+         objective=0, loss_mode=0, std_unbiased=True):
     wl = synth.generate(cfg, seed=seed)
-    dw = DeviceWorkload(wl, mask=mask, chunk_rows=chunk_rows)
+    dw = DeviceWorkload(wl, mask=mask, chunk_rows=chunk_rows, objective=objective, loss_mode=loss_mode,
+                        std_unbiased=std_unbiased)
     (dw.fwd() if fwd_only else dw.fwd_bwd(loss_scale))
     res = dw.results()
     exp = oracle.expected(wl, mask=res["mask"], eval_rows=eval_rows, vrows=vrows,
-                          want_dH=not fwd_only, want_dW=not fwd_only)
+                          want_dH=not fwd_only, want_dW=not fwd_only, objective=objective,
+                          loss_mode=loss_mode, std_unbiased=std_unbiased)
     assert np.array_equal(res["adv"].view(np.uint32), exp["adv"].view(np.uint32))
     return wl, dw, res, exp
 
@@ -204,6 +207,26 @@ def test_deterministic_and_fwd_matches_fwd_bwd():
     assert torch.equal(a["rs"], dw.row_stats)
     assert torch.equal(a["dH"].view(torch.int16), dw.dH.view(torch.int16))
     assert torch.equal(a["dW"].view(torch.int32), dw.dW.view(torch.int32))
+
+
+@pytest.mark.parametrize("objective", ["grpo", "no_detach", "reverse_kl_q", "forward_kl"])
+@pytest.mark.parametrize("loss_mode", [0, 1])
+def test_objective_variants_and_means(objective, loss_mode):
+    # several prompt groups, one fully masked completion, KL large enough to matter
+    cfg = synth.make_config("tiny", n_groups=3, G=4, L=150, d=192, V=1000, len_lo=1, len_hi=150,
+                            n_zero_seq=1, sigma_ref=0.3)
+    _, _, res, exp = _run(cfg, seed=31, chunk_rows=256, objective=objective, loss_mode=loss_mode)
+    assert_fwd_parity(res, exp)
+    assert_grad_parity(res, exp)
+
+
+@pytest.mark.parametrize("fwd_only", [True, False])
+def test_population_std_and_sequence_mean_forward(fwd_only):
+    cfg = synth.make_config("tiny", n_groups=2, G=8, L=96, d=128, V=2048, len_lo=0, len_hi=96)
+    _, _, res, exp = _run(cfg, seed=37, std_unbiased=False, loss_mode=1, fwd_only=fwd_only)
+    assert_fwd_parity(res, exp)
+    if not fwd_only:
+        assert_grad_parity(res, exp)
 
 
 def test_all_rows_masked():

@@ -198,8 +198,8 @@ def test_row_terms_against_numpy_scipy():
     assert np.allclose(t["lse_ref"], lr, rtol=0, atol=1e-12)
     assert np.allclose(t["q"], q, atol=1e-12) and np.allclose(t["p"], p, atol=1e-12)
     # KL estimator: e^x - x - 1 >= 0
-    assert np.all(t["kl"] >= 0)
-    assert np.allclose(t["kl"], np.exp(x) - x - 1, atol=1e-12)
+    assert np.all(t["pen"] >= 0)
+    assert np.allclose(t["pen"], np.exp(x) - x - 1, atol=1e-12)
     assert np.allclose(t["ell"], -A + 0.04 * (np.exp(x) - x - 1), atol=1e-12)
     assert np.allclose(t["g"], -A + 0.04 * (1 - np.exp(x)), atol=1e-12)
 
@@ -213,7 +213,7 @@ def test_kl_small_argument_taylor():
     t = oracle.row_terms(h_pol, h_ref, W, "f64", tok, adv, L, rows)
     x = t["p"] - t["q"]
     assert np.all(np.abs(x) < 1e-5) and np.any(np.abs(x) > 1e-9)
-    assert np.allclose(t["kl"], x * x / 2 + x ** 3 / 6, rtol=1e-6, atol=0)
+    assert np.allclose(t["pen"], x * x / 2 + x ** 3 / 6, rtol=1e-6, atol=0)
 
 
 def test_policy_equals_reference_closed_form():
@@ -224,7 +224,7 @@ def test_policy_equals_reference_closed_form():
     mask = oracle.build_mask(wl.lengths, cfg.L)
     rows = oracle.valid_rows(mask)
     t = oracle.row_terms(wl.h_pol, wl.h_pol, wl.W, "bf16", wl.tokens, adv, cfg.L, rows)
-    assert np.all(t["kl"] == 0.0)
+    assert np.all(t["pen"] == 0.0)
     assert np.array_equal(t["g"], -adv[rows // cfg.L].astype(np.float64))
     loss, nv = oracle.loss(wl.h_pol, wl.h_pol, wl.W, "bf16", wl.tokens, mask, adv, cfg.L)
     lens = wl.lengths.astype(np.float64)
@@ -320,6 +320,82 @@ def test_without_detach_policy_gradient_vanishes():
             fd = _fd(Jnd, h_pol, (r, k))
             assert abs(fd - dH_kl[i, k]) <= 1e-6 * max(1e-3, abs(dH_kl[i, k])) + 1e-10
     assert np.max(np.abs(dH_full - dH_kl)) > 1e-3
+
+
+def _fd_check(fun, h_pol, W, rows, dH, dW):
+    for i, r in enumerate(rows):
+        for k in range(h_pol.shape[1]):
+            fd = _fd(fun, h_pol, (r, k))
+            assert abs(fd - dH[i, k]) <= 1e-6 * max(1e-3, abs(dH[i, k])) + 1e-10, (r, k, fd, dH[i, k])
+    for v in range(W.shape[0]):
+        for k in range(W.shape[1]):
+            fd = _fd(fun, W, (v, k))
+            assert abs(fd - dW[v, k]) <= 1e-6 * max(1e-3, abs(dW[v, k])) + 1e-10, (v, k, fd, dW[v, k])
+
+
+@pytest.mark.parametrize("objective", ["grpo", "no_detach", "reverse_kl_q", "forward_kl"])
+@pytest.mark.parametrize("loss_mode", ["token_mean", "sequence_mean"])
+def test_variant_gradients_finite_differences(objective, loss_mode):
+    """Each objective variant and each mean: g and the weights give the surrogate's gradient."""
+    h_pol, h_ref, W, tok, adv, mask, L = _tiny_problem(seed=21, G=3, L=3, d=3, V=4, lens=(1, 3, 2), ref_noise=0.5)
+    rows = oracle.valid_rows(mask)
+    w = oracle.row_weights(rows, L, loss_mode)
+    t = oracle.row_terms(h_pol, h_ref, W, "f64", tok, adv, L, rows, objective=objective)
+    c = None if objective == "no_detach" else t["q"].copy()
+    W_ref = W.copy()
+    loss, _ = oracle.loss(h_pol, h_ref, W, "f64", tok, mask, adv, L, objective=objective, loss_mode=loss_mode)
+    J0 = oracle.surrogate(h_pol, h_ref, W, "f64", tok, adv, L, rows, c, w, W_ref=W_ref, objective=objective)
+    assert abs(J0 - loss) <= 1e-14 * max(1, abs(loss))          # surrogate value = the loss
+    dH, dW = oracle.grad(h_pol, W, "f64", tok, rows, t["lse_pol"], t["g"], w)
+
+    def J():
+        return oracle.surrogate(h_pol, h_ref, W, "f64", tok, adv, L, rows, c, w, W_ref=W_ref, objective=objective)
+
+    _fd_check(J, h_pol, W, rows, dH, dW)
+
+
+def test_variant_values():
+    """Penalty terms of the variants against their definitions at chosen x = p - q."""
+    h_pol, h_ref, W, tok, adv, mask, L = _tiny_problem(seed=22, ref_noise=0.7)
+    rows = np.arange(h_pol.shape[0], dtype=np.int32)
+    base = oracle.row_terms(h_pol, h_ref, W, "f64", tok, adv, L, rows, objective="grpo")
+    x = base["p"] - base["q"]
+    assert np.any(np.abs(x) > 0.1)
+    k_rev = np.exp(x) - x - 1
+    A = adv[rows // L].astype(np.float64)
+    nd = oracle.row_terms(h_pol, h_ref, W, "f64", tok, adv, L, rows, objective="no_detach")
+    assert np.array_equal(nd["ell"], base["ell"])                       # same value
+    assert np.allclose(nd["g"], 0.04 * (1 - np.exp(x)), atol=1e-15)     # the A term has no gradient
+    rq = oracle.row_terms(h_pol, h_ref, W, "f64", tok, adv, L, rows, objective="reverse_kl_q")
+    assert np.allclose(rq["pen"], np.exp(base["q"]) * k_rev, rtol=1e-12, atol=1e-15)
+    fk = oracle.row_terms(h_pol, h_ref, W, "f64", tok, adv, L, rows, objective="forward_kl")
+    assert np.allclose(fk["pen"], np.exp(-x) + x - 1, rtol=1e-10, atol=1e-15)
+    assert np.all(fk["pen"] >= 0) and np.all(rq["pen"] >= 0)
+    for t in (nd, rq, fk):
+        assert np.allclose(t["ell"], -A + 0.04 * t["pen"], atol=1e-15)
+    # policy = reference: every penalty vanishes
+    for obj in ("grpo", "no_detach", "reverse_kl_q", "forward_kl"):
+        same = oracle.row_terms(h_pol, h_pol, W, "f64", tok, adv, L, rows, objective=obj)
+        assert np.all(same["pen"] == 0)
+
+
+def test_sequence_mean_closed_form():
+    """Policy = reference under the per-completion mean: loss = -mean of A over completions with tokens."""
+    wl = synth.generate(synth.make_config("tiny", n_zero_seq=1), seed=8)
+    cfg = wl.cfg
+    adv = oracle.group_advantages(wl.rewards, 1, cfg.G)
+    mask = oracle.build_mask(wl.lengths, cfg.L)
+    loss, _ = oracle.loss(wl.h_pol, wl.h_pol, wl.W, "bf16", wl.tokens, mask, adv, cfg.L, loss_mode="sequence_mean")
+    active = wl.lengths > 0
+    assert active.sum() == cfg.G - 1
+    closed = -float(np.mean(adv[active].astype(np.float64)))
+    assert abs(loss - closed) <= 1e-15
+    rows = oracle.valid_rows(mask)
+    w = oracle.row_weights(rows, cfg.L, "sequence_mean")
+    assert abs(w.sum() - 1.0) <= 1e-15
+    for i in np.flatnonzero(active):
+        sel = (rows // cfg.L) == i
+        assert np.allclose(w[sel], 1.0 / (active.sum() * wl.lengths[i]), rtol=1e-15)
 
 
 def test_expected_bundle_consistency():
