@@ -406,6 +406,7 @@ def run_ours(args, ranks):
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                 "frac": achieved / sustained, "peak_kind": f"bf16 dense sustained, {pk_kind}",
                 "traffic": ncu_traffic(dom, cfg.name),
+                "traffic_per": "full chunk launch (ncu DRAM read+write bytes)",
                 "flops_per_launch": flops_kind[dom] * args.steps / dom_n, "ms_per_launch": dom_ms / dom_n}
     useful = 8.0 * n_valid * V * d
     t_step = ms_step / 1e3

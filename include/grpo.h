@@ -131,7 +131,8 @@ int grpo_valid_rows(const uint8_t* mask, const grpo_shape* shape, int32_t* rows_
 
 /* Forward pass of the linear GRPO loss ("Long-context GRPO", section 2: the
  * memory-efficient linear algorithm; section 4: the objective, the detach
- * factor and the logsumexp trick).
+ * factor and the logsumexp trick).  Runs the same chunked kernels as
+ * grpo_loss_fwd_bwd, without the backward.
  *   h_pol, h_ref [N x d], W [V x d]          (dtype; device, read)
  *   tokens [N] int32 in [0, V)               (device, read; masked rows too)
  *   mask [N] uint8, nonzero = completion token (device, read)
@@ -159,9 +160,9 @@ int grpo_loss_fwd(const void* h_pol, const void* h_ref, const void* W, const int
  *   found_inf: one int32 (device) <- 1 if any scaled gradient value (the
  *               16-bit dlogits, dH or dW) is not finite, else 0.  The caller
  *               lowers the scale and calls again when it is set.
- * The loss matches grpo_loss_fwd's to fp32 rounding (the two split the
- * vocabulary differently); every output is bitwise reproducible from run to
- * run (fixed reduction orders, no floating-point atomics). */
+ * The loss and row_stats equal grpo_loss_fwd's bit for bit; every output is
+ * bitwise reproducible from run to run (fixed reduction orders, no
+ * floating-point atomics). */
 int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
                       const uint8_t* mask, const float* adv, const grpo_shape* shape,
                       float loss_scale, void* workspace, size_t ws_bytes, float* loss_out,
@@ -178,7 +179,9 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
  * Same inputs and outputs as grpo_loss_fwd, without the workspace: the
  * library uses an 8 MiB array of its own, held on every GPU that loads the
  * library until the process exits.  It allocates nothing and calls no
- * allocating routine.
+ * allocating routine.  It runs all rows at once on single-SM kernels, so its
+ * results equal grpo_loss_fwd's up to fp32 rounding (the vocabulary is split
+ * differently).
  *   Limit: N = n_groups*G*L <= 32768 rows; larger shapes are rejected with
  *   GRPO_ERR_WORKSPACE before anything is launched.
  *   The first call on a device looks up the array's device address (a

@@ -324,6 +324,108 @@ int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     return run_loss_reduce(in, L, w, st);
 }
 
+// The chunked path: for each chunk of masked-in rows, gather compact copies of
+// its h_pol / h_ref rows, run the SM-pair forward, merge per row; with a
+// backward, keep the policy exponentials and turn them into dlogits, dH and
+// dW.  Then reduce the loss.  Uses the whole workspace.
+struct Backward {
+    float loss_scale;
+    void* dH;
+    float* dW;
+    int32_t* found_inf;
+};
+
+int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cudaStream_t st, const Backward* bwd) {
+    const grpo_shape& s = *in.shape;
+    const bool bf16 = s.dtype == GRPO_BF16;
+    char* w = static_cast<char*>(in.ws);
+    int* counts = reinterpret_cast<int*>(w + L.counts);
+    int rc = run_index(in, L, w, st);
+    if (rc != GRPO_OK) return rc;
+    // masked rows: objective 0; with a backward: found_inf <- 0, dW <- 0 when no row
+    // is masked in, dH rows of masked rows <- 0
+    if (launch(GRPO_PROF_CLEAR, st, [&] {
+            return launch_rows_init(in.mask, L.N, reinterpret_cast<float*>(w + L.ell), in.row_stats, st);
+        }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (bwd) {
+        if (launch(GRPO_PROF_CLEAR, st, [&] {
+                return launch_clear_grads(counts, bwd->found_inf, bwd->dW, static_cast<int64_t>(s.V) * s.d, st);
+            }) != cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_CLEAR, st, [&] { return launch_zero_masked_rows(in.mask, L.N, s.d, bwd->dH, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+    }
+
+    CUtensorMap mW_k, mW_mn, mHc_k, mHcr_k, mHc_mn, mDS_k, mDS_mn;
+    void* hc = w + L.hc;
+    void* hcr = w + L.hcr;
+    void* ds = w + L.ds;
+    // W tiles for the pair forward: each CTA of a pair loads 128 of the 256 vocabulary rows
+    if (!make_map(&mW_k, in.W, bf16, s.d, s.V, s.d, kBK, kBN / 2) ||
+        !make_map(&mW_mn, in.W, bf16, s.d, s.V, s.d, 64, kBK) || !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
+        !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
+        !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
+        !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
+        !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK))
+        return GRPO_ERR_LAUNCH;
+
+    FwdParams fp = fwd_params(in, L, w);
+    fp.tiles = nullptr;                                  // chunk mode
+    fp.part = reinterpret_cast<float4*>(w + L.partc);
+    fp.S = L.Sc;
+    fp.nps = L.npsc;
+    // the exponentials are kept only when a backward follows
+    fp.E = bwd ? static_cast<uint16_t*>(ds) : nullptr;
+    fp.mx = bwd ? reinterpret_cast<float*>(w + L.mx) : nullptr;
+
+    ChunkParams cp;
+    cp.counts = counts;
+    cp.rows = reinterpret_cast<const int*>(w + L.rows);
+    cp.tokens = in.tokens;
+    cp.lse = reinterpret_cast<const float*>(w + L.lse);
+    cp.gco = reinterpret_cast<const float*>(w + L.gco);
+    cp.zt = reinterpret_cast<const float2*>(w + L.zt);
+    cp.mx = reinterpret_cast<const float*>(w + L.mx);
+    cp.scale = bwd ? bwd->loss_scale : 1.f;
+    cp.V = s.V;
+    cp.d = s.d;
+    cp.V_pad = L.V_pad;
+    cp.nc32 = L.nc32;
+    cp.dS = static_cast<uint16_t*>(ds);
+    cp.dH = bwd ? static_cast<uint16_t*>(bwd->dH) : nullptr;
+    cp.dW = bwd ? bwd->dW : nullptr;
+    cp.sched = nullptr;
+    cp.found_inf = bwd ? bwd->found_inf : nullptr;
+    cp.status = in.status;
+    const int64_t max_chunks = (L.N + L.R - 1) / L.R;
+    for (int64_t c = 0; c < max_chunks; ++c) {
+        const int ci = static_cast<int>(c);
+        cp.chunk = ci;
+        fp.chunk = ci;
+        fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
+        const MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
+        if (launch(GRPO_PROF_GATHER, st,
+                   [&] { return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, st); }) != cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_FWD, st,
+                   [&] { return launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) != cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
+        if (!bwd) continue;
+        if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+        if (launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st); }) !=
+            cudaSuccess)
+            return GRPO_ERR_LAUNCH;
+    }
+    return run_loss_reduce(in, L, w, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -407,7 +509,7 @@ int grpo_loss_fwd(const void* h_pol, const void* h_ref, const void* W, const int
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != GRPO_OK) return rc;
-    return run_forward(in, L, dev, reinterpret_cast<cudaStream_t>(stream));
+    return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens, const uint8_t* mask,
@@ -424,90 +526,8 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != GRPO_OK) return rc;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const grpo_shape& s = *shape;
-    const bool bf16 = s.dtype == GRPO_BF16;
-    char* w = static_cast<char*>(workspace);
-    int* counts = reinterpret_cast<int*>(w + L.counts);
-
-    rc = run_index(in, L, w, st);
-    if (rc != GRPO_OK) return rc;
-    // found_inf <- 0 (dW <- 0 when no row is masked in); masked rows: objective 0, dH rows 0
-    if (launch(GRPO_PROF_CLEAR, st,
-               [&] { return launch_clear_grads(counts, found_inf, dW, static_cast<int64_t>(s.V) * s.d, st); }) !=
-        cudaSuccess)
-        return GRPO_ERR_LAUNCH;
-    if (launch(GRPO_PROF_CLEAR, st, [&] {
-            return launch_rows_init(mask, L.N, reinterpret_cast<float*>(w + L.ell), row_stats, st);
-        }) != cudaSuccess)
-        return GRPO_ERR_LAUNCH;
-    if (launch(GRPO_PROF_CLEAR, st, [&] { return launch_zero_masked_rows(mask, L.N, s.d, dH, st); }) != cudaSuccess)
-        return GRPO_ERR_LAUNCH;
-
-    CUtensorMap mW_k, mW_mn, mHc_k, mHcr_k, mHc_mn, mDS_k, mDS_mn;
-    void* hc = w + L.hc;
-    void* hcr = w + L.hcr;
-    void* ds = w + L.ds;
-    // W tiles for the pair forward: each CTA of a pair loads 128 of the 256 vocabulary rows
-    if (!make_map(&mW_k, W, bf16, s.d, s.V, s.d, kBK, kBN / 2) ||
-        !make_map(&mW_mn, W, bf16, s.d, s.V, s.d, 64, kBK) || !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
-        !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
-        !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
-        !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
-        !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK))
-        return GRPO_ERR_LAUNCH;
-
-    FwdParams fp = fwd_params(in, L, w);
-    fp.tiles = nullptr;                                  // chunk mode
-    fp.part = reinterpret_cast<float4*>(w + L.partc);
-    fp.S = L.Sc;
-    fp.nps = L.npsc;
-    fp.E = static_cast<uint16_t*>(ds);
-    fp.mx = reinterpret_cast<float*>(w + L.mx);
-
-    ChunkParams cp;
-    cp.counts = counts;
-    cp.rows = reinterpret_cast<const int*>(w + L.rows);
-    cp.tokens = tokens;
-    cp.lse = reinterpret_cast<const float*>(w + L.lse);
-    cp.gco = reinterpret_cast<const float*>(w + L.gco);
-    cp.zt = reinterpret_cast<const float2*>(w + L.zt);
-    cp.mx = reinterpret_cast<const float*>(w + L.mx);
-    cp.scale = loss_scale;
-    cp.V = s.V;
-    cp.d = s.d;
-    cp.V_pad = L.V_pad;
-    cp.nc32 = L.nc32;
-    cp.dS = static_cast<uint16_t*>(ds);
-    cp.dH = static_cast<uint16_t*>(dH);
-    cp.dW = dW;
-    cp.sched = nullptr;
-    cp.found_inf = found_inf;
-    cp.status = status;
-    const int64_t max_chunks = (L.N + L.R - 1) / L.R;
-    for (int64_t c = 0; c < max_chunks; ++c) {
-        const int ci = static_cast<int>(c);
-        cp.chunk = ci;
-        fp.chunk = ci;
-        fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
-        const MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
-        if (launch(GRPO_PROF_GATHER, st, [&] { return launch_gather_rows(cp, h_pol, hc, h_ref, hcr, L.R, st); }) !=
-            cudaSuccess)
-            return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_FWD, st,
-                   [&] { return launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) != cudaSuccess)
-            return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
-            return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
-            cudaSuccess)
-            return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st); }) !=
-            cudaSuccess)
-            return GRPO_ERR_LAUNCH;
-    }
-    return run_loss_reduce(in, L, w, st);
+    const Backward bwd{loss_scale, dH, dW, found_inf};
+    return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), &bwd);
 }
 
 const char* grpo_status_string(int status) {
