@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of one oracle sample")
+    ap.add_argument("--forward", action="store_true",
+                    help="time the forward-only entry points (bf16 and e4m3 inputs) instead of fwd+bwd")
     return ap.parse_args()
 
 
@@ -442,6 +444,72 @@ def run_ours(args, ranks):
         print(json.dumps(line), flush=True)
 
 
+def run_forward_modes(args, ranks):
+    """Forward-only throughput: grpo_loss_fwd on bf16 inputs and grpo_loss_fwd_fp8 on
+    the same workload quantised to e4m3 (one scale per tensor)."""
+    import numpy as np
+    import torch
+
+    import rl_fine_tuning_gb300 as rg
+    import synth
+
+    torch.cuda.set_device(ranks.local)
+    rg.load(build_if_missing=True)
+    cfg = synth.make_config(args.config)
+    n_valid = int(np.minimum(np.maximum(synth.lengths_for(cfg, 0), 0), cfg.L).sum())
+    stream = torch.cuda.current_stream()
+    out = {}
+    for mode in ("bf16", "e4m3"):
+        if mode == "bf16":
+            wl = synth.generate(cfg, seed=0)
+            mats = [torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16) for a in (wl.h_pol, wl.h_ref, wl.W)]
+            shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.BF16, beta=cfg.beta, eps=cfg.eps)
+        else:
+            wl = synth.generate_e4m3(cfg, seed=0)
+            mats = [torch.from_numpy(a).cuda() for a in (wl.h_pol, wl.h_ref, wl.W)]
+            shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.E4M3, beta=cfg.beta, eps=cfg.eps)
+        tokens, lengths, rewards = (torch.from_numpy(a).cuda() for a in (wl.tokens, wl.lengths, wl.rewards))
+        adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
+        mask = torch.empty(cfg.N, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(rg.grpo_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+        loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def step():
+            rg.grpo_group_advantages(rewards, cfg.n_groups, cfg.G, cfg.eps, True, adv)
+            rg.grpo_build_mask(lengths, shape, mask)
+            if mode == "bf16":
+                rg.grpo_loss_fwd(*mats, tokens, mask, adv, shape, ws, loss, None, status)
+            else:
+                rg.grpo_loss_fwd_fp8(*mats, *wl.extra["scales"], tokens, mask, adv, shape, ws, loss, None, status)
+
+        for _ in range(max(args.warmup, 1)):
+            step()
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise SystemExit(f"device status {int(status.item())}")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        flops = 4.0 * n_valid * cfg.V * cfg.d
+        out[mode] = {"ms_per_step": ms, "tokens_per_s": n_valid / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
+                     "loss": float(loss.item())}
+        del mats, ws, wl
+        torch.cuda.empty_cache()
+    pk, pk_kind = peaks()
+    line = {"metric": "GRPO loss forward tokens/s (bf16 and e4m3 inputs)", "value": out["e4m3"]["tokens_per_s"],
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": out["e4m3"]["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": cfg_dict(cfg, {"n_valid": n_valid}),
+            "forward": out, "bf16_peak_tflops": pk.get("bf16_tflops"), "peaks": pk_kind}
+    if ranks.rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def cpu_baseline(cfg, wl, args):
     """The oracle, as it stands, on the host cores: a bounded sample of rows."""
     import oracle
@@ -464,6 +532,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, ranks)
+        elif args.forward:
+            run_forward_modes(args, ranks)
         else:
             run_ours(args, ranks)
     finally:

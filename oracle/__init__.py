@@ -50,6 +50,8 @@ def _L():
         lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_f16_to_f64.restype = f64
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_e4m3_to_f64.restype = f64
+        lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_group_advantages.argtypes = [p, i32, i32, ctypes.c_float, i32, p]
         lib.oracle_build_mask.argtypes = [p, i32, i32, p]
         lib.oracle_valid_rows.restype = i64
@@ -89,6 +91,23 @@ def _mat(a, dtype):
     if dtype == "f64":
         return np.ascontiguousarray(a, np.float64)
     return np.ascontiguousarray(a, np.uint16)
+
+
+def e4m3_values(codes, scale):
+    """e4m3 codes -> float64 values code * scale (exact in fp64), via the oracle's decoder."""
+    lut = np.array([_L().oracle_e4m3_to_f64(i) for i in range(256)], np.float64)
+    return lut[np.ascontiguousarray(codes, np.uint8)] * float(scale)
+
+
+def dequantized_workload(wl):
+    """A copy of an e4m3 workload whose matrices are the exact float64 values."""
+    from copy import copy
+    s_pol, s_ref, s_w = wl.extra["scales"]
+    out = copy(wl)
+    out.h_pol = e4m3_values(wl.h_pol, s_pol)
+    out.h_ref = e4m3_values(wl.h_ref, s_ref)
+    out.W = e4m3_values(wl.W, s_w)
+    return out
 
 
 def group_advantages(rewards, n_groups, G, eps=1e-4, std_unbiased=True):
@@ -222,13 +241,14 @@ def expected(wl, eval_rows=None, vrows=None, mask=None, want_dH=True, want_dW=Tr
     full = eval_rows is None
     rows = rows_all if full else np.ascontiguousarray(eval_rows, np.int32)
     w = w_all if full else w_all[np.searchsorted(rows_all, rows)]
-    terms = row_terms(wl.h_pol, wl.h_ref, wl.W, cfg.dtype, wl.tokens, adv, cfg.L, rows, cfg.beta,
+    mtype = "f64" if wl.h_pol.dtype == np.float64 else cfg.dtype
+    terms = row_terms(wl.h_pol, wl.h_ref, wl.W, mtype, wl.tokens, adv, cfg.L, rows, cfg.beta,
                       objective=objective)
     out = dict(adv=adv, mask=mask, rows=rows_all, n_valid=n_valid, w=w, eval_rows=rows, terms=terms)
     if full:
         out["loss"] = reduce_loss(terms["ell"], rows_all, cfg.L, loss_mode)
     if want_dH or want_dW:
-        dH, dW = grad(wl.h_pol, wl.W, cfg.dtype, wl.tokens, rows, terms["lse_pol"], terms["g"], w,
+        dH, dW = grad(wl.h_pol, wl.W, mtype, wl.tokens, rows, terms["lse_pol"], terms["g"], w,
                       want_dH=want_dH, vrows=vrows, want_dW=want_dW and full)
         out["dH"] = dH
         out["dW"] = dW

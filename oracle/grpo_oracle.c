@@ -79,6 +79,19 @@ double oracle_f16_to_f64(uint16_t b) {
     return sign ? -v : v;
 }
 
+/* OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite 448, smallest subnormal 2^-9. */
+double oracle_e4m3_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 15;
+    int m = b & 7;
+    double v;
+    if (e == 15 && m == 7) v = NAN;
+    else if (e == 0) v = ldexp((double)m, -9);
+    else v = ldexp((double)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
 static inline double ld(const void* p, int type, size_t i) {
     if (type == OR_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[i]);
     if (type == OR_F16) return oracle_f16_to_f64(((const uint16_t*)p)[i]);

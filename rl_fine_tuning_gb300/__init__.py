@@ -24,7 +24,7 @@ __all__ = [
 # kernel kinds of the diagnostics interface, in the order of the GRPO_PROF_* enum
 PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "dlogits", "dh", "dw")
 
-BF16, FP16 = 0, 1
+BF16, FP16, E4M3 = 0, 1, 2
 TOKEN_MEAN, SEQUENCE_MEAN = 0, 1
 OBJECTIVES = {"grpo": 0, "no_detach": 1, "reverse_kl_q": 2, "forward_kl": 3}
 
@@ -205,3 +205,15 @@ def grpo_loss_fwd_noalloc(h_pol, h_ref, W, tokens, mask, adv, shape, loss_out, r
         fn.restype = ctypes.c_int
     _check(fn(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv), ctypes.byref(shape),
               _ptr(loss_out), _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_noalloc")
+
+
+def grpo_loss_fwd_fp8(h_pol, h_ref, W, scale_h_pol, scale_h_ref, scale_w, tokens, mask, adv, shape, workspace,
+                      loss_out, row_stats, status, stream=None):
+    fn = load().grpo_loss_fwd_fp8
+    if fn.argtypes is None:
+        p, f = ctypes.c_void_p, ctypes.c_float
+        fn.argtypes = [p, p, p, f, f, f, p, p, p, ctypes.POINTER(GrpoShape), p, ctypes.c_size_t, p, p, p, p]
+        fn.restype = ctypes.c_int
+    _check(fn(_ptr(h_pol), _ptr(h_ref), _ptr(W), float(scale_h_pol), float(scale_h_ref), float(scale_w), _ptr(tokens),
+              _ptr(mask), _ptr(adv), ctypes.byref(shape), _ptr(workspace), _nbytes(workspace), _ptr(loss_out),
+              _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_fp8")

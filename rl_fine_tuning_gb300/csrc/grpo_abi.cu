@@ -131,6 +131,21 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint64
     return r == CUDA_SUCCESS;
 }
 
+// 2-D row-major matrix of 8-bit elements (E4M3 codes), 128-byte swizzled boxes
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_cols,
+                 uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int chunk_rows_of(const grpo_shape& s) {
     int r = s.chunk_rows > 0 ? s.chunk_rows : kDefaultChunkRows;
     r = (r + kBM - 1) / kBM * kBM;
@@ -266,6 +281,7 @@ FwdParams fwd_params(const Inputs& in, const WsLayout& L, char* w) {
     fp.n_ntiles = L.n_ntiles;
     fp.V_pad = L.V_pad;
     fp.nc32 = L.nc32;
+    fp.zscale[0] = fp.zscale[1] = 1.f;
     fp.status = in.status;
     return fp;
 }
@@ -335,9 +351,16 @@ struct Backward {
     int32_t* found_inf;
 };
 
-int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cudaStream_t st, const Backward* bwd) {
+// per-tensor scales of E4M3 inputs (forward only)
+struct E4m3Scales {
+    float h_pol, h_ref, w;
+};
+
+int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cudaStream_t st, const Backward* bwd,
+                const E4m3Scales* f8 = nullptr) {
     const grpo_shape& s = *in.shape;
     const bool bf16 = s.dtype == GRPO_BF16;
+    const int row_bytes = f8 ? s.d : 2 * s.d;
     char* w = static_cast<char*>(in.ws);
     int* counts = reinterpret_cast<int*>(w + L.counts);
     int rc = run_index(in, L, w, st);
@@ -363,13 +386,20 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     void* hcr = w + L.hcr;
     void* ds = w + L.ds;
     // W tiles for the pair forward: each CTA of a pair loads 128 of the 256 vocabulary rows
-    if (!make_map(&mW_k, in.W, bf16, s.d, s.V, s.d, kBK, kBN / 2) ||
-        !make_map(&mW_mn, in.W, bf16, s.d, s.V, s.d, 64, kBK) || !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
-        !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
-        !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
-        !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
-        !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK))
+    if (f8) {
+        // 8-bit inputs: a K-stage is one 128-byte span of 128 elements
+        if (!make_map_u8(&mW_k, in.W, s.d, s.V, s.d, 128, kBN / 2) ||
+            !make_map_u8(&mHc_k, hc, s.d, L.R, s.d, 128, kBM) || !make_map_u8(&mHcr_k, hcr, s.d, L.R, s.d, 128, kBM))
+            return GRPO_ERR_LAUNCH;
+    } else if (!make_map(&mW_k, in.W, bf16, s.d, s.V, s.d, kBK, kBN / 2) ||
+               !make_map(&mW_mn, in.W, bf16, s.d, s.V, s.d, 64, kBK) ||
+               !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
+               !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
+               !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
+               !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
+               !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK)) {
         return GRPO_ERR_LAUNCH;
+    }
 
     FwdParams fp = fwd_params(in, L, w);
     fp.tiles = nullptr;                                  // chunk mode
@@ -379,6 +409,10 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     // the exponentials are kept only when a backward follows
     fp.E = bwd ? static_cast<uint16_t*>(ds) : nullptr;
     fp.mx = bwd ? reinterpret_cast<float*>(w + L.mx) : nullptr;
+    if (f8) {
+        fp.zscale[0] = f8->h_pol * f8->w;
+        fp.zscale[1] = f8->h_ref * f8->w;
+    }
 
     ChunkParams cp;
     cp.counts = counts;
@@ -407,10 +441,13 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
         const MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
         if (launch(GRPO_PROF_GATHER, st,
-                   [&] { return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, st); }) != cudaSuccess)
+                   [&] { return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, row_bytes, st); }) !=
+            cudaSuccess)
             return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_FWD, st,
-                   [&] { return launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st); }) != cudaSuccess)
+        if (launch(GRPO_PROF_FWD, st, [&] {
+                return f8 ? launch_fwd_pair_e4m3(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, st)
+                          : launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st);
+            }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
         if (!bwd) continue;
@@ -449,8 +486,10 @@ void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, gr
 
 size_t grpo_workspace_bytes(const grpo_shape* shape) {
     if (!shape) return 0;
+    grpo_shape s = *shape;
+    if (s.dtype == GRPO_E4M3) s.dtype = GRPO_BF16;   // same layout; the 8-bit chunk copies use half
     WsLayout L;
-    if (!ws_layout(*shape, &L)) return 0;
+    if (!ws_layout(s, &L)) return 0;
     return L.total;
 }
 
@@ -528,6 +567,30 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     if (rc != GRPO_OK) return rc;
     const Backward bwd{loss_scale, dH, dW, found_inf};
     return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), &bwd);
+}
+
+int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float scale_h_pol, float scale_h_ref,
+                      float scale_w, const int32_t* tokens, const uint8_t* mask, const float* adv,
+                      const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out, float* row_stats,
+                      int32_t* status, grpo_stream_t stream) {
+    if (!shape) return GRPO_ERR_SHAPE;
+    if (shape->dtype != GRPO_E4M3) return GRPO_ERR_DTYPE;
+    if (shape->d % 128 != 0) return GRPO_ERR_SHAPE;
+    if (!(scale_h_pol > 0.f) || !(scale_h_ref > 0.f) || !(scale_w > 0.f) || !std::isfinite(scale_h_pol) ||
+        !std::isfinite(scale_h_ref) || !std::isfinite(scale_w))
+        return GRPO_ERR_SHAPE;
+    // the workspace layout is the 16-bit one (the 8-bit chunk copies use half of it)
+    grpo_shape s16 = *shape;
+    s16.dtype = GRPO_BF16;
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, &s16, workspace, ws_bytes, loss_out, row_stats, status};
+    WsLayout L;
+    int rc = validate(in, &L);
+    if (rc != GRPO_OK) return rc;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    const E4m3Scales f8{scale_h_pol, scale_h_ref, scale_w};
+    return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr, &f8);
 }
 
 const char* grpo_status_string(int status) {

@@ -65,6 +65,7 @@ struct FwdParams {
     uint16_t* E;            // [R x V_pad] bf16 exp(z_pol - m) (chunk mode, may be nullptr)
     float* mx;              // [R x nc32] running max after each 32-column group (chunk mode)
     int* sched;             // zeroed work counter of this launch
+    float zscale[2];        // logits = zscale * accumulator (policy, reference); 1 unless 8-bit inputs
     int64_t N;
     int chunk;
     int V, d, S, nps, n_ntiles, V_pad, nc32;
@@ -125,7 +126,7 @@ cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* 
 cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, int nblk, const int* counts,
                                float* loss_out, cudaStream_t st);
 cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
-                               cudaStream_t st);
+                               int row_bytes, cudaStream_t st);
 cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, cudaStream_t st);
 cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, cudaStream_t st);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st);
@@ -135,6 +136,8 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtenso
 // CTA-pair (M=256) variants: forward of a chunk, dH, dW
 cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
                             const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
+cudaError_t launch_fwd_pair_e4m3(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
+                                 const CUtensorMap& mW, int n_sm, cudaStream_t st);
 cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm,
                            bool bf16, cudaStream_t st);
 cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,

@@ -450,8 +450,8 @@ __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restr
 }
 
 cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
-                               cudaStream_t st) {
-    const int vpr = p.d / 8;
+                               int row_bytes, cudaStream_t st) {
+    const int vpr = row_bytes / 16;
     const int64_t total = static_cast<int64_t>(R) * vpr;
     int blocks = static_cast<int>((total + 255) / 256);
     if (blocks > 152 * 16) blocks = 152 * 16;

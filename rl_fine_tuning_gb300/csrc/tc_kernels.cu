@@ -598,6 +598,11 @@ struct FwdPairT {
             if (col0 >= p.V) break;
             float v[32];
             tmem_ld32(tacc + c * 32, v);
+            const float zs = p.zscale[rank];
+            if (zs != 1.f) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= zs;
+            }
             const int nvalid = p.V - col0;
             if (nvalid < 32) {
 #pragma unroll
@@ -640,6 +645,31 @@ struct FwdPairT {
         float* part = reinterpret_cast<float*>(p.part + static_cast<int64_t>(e.slot) * p.S + e.split);
         *reinterpret_cast<float2*>(part + 2 * rank) = make_float2(e.m, e.s);
         if (e.found) reinterpret_cast<float*>(p.zt + e.t)[rank] = e.zt;
+    }
+};
+
+// The chunk forward on E4M3 inputs: the same tiles, byte for byte (a 128-byte
+// row holds 128 elements), a K-stage of 128 elements, four K=32 MMAs of kind
+// f8f6f4 per stage, and the per-tensor scales applied to the accumulator.
+struct FwdPairF8T : FwdPairT {
+    static constexpr int kStageElems = 128;
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!FwdPairT::setup(p, sc)) return false;
+        sc.ks = p.d / kStageElems;
+        return true;
+    }
+    __device__ static void load(const Params&, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap* mA2, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(rank == 0 ? mA : mA2, bar, st, k * kStageElems, c.m0);
+        tma_load_2d_pair(mB, bar, st + 16384, k * kStageElems, c.n0 + rank * 128);
+    }
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_e4m3(256, 256);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_pair_f8(acc, desc_kmajor(st + kk * 32), desc_kmajor(st + 16384 + kk * 32), idesc,
+                         (first && kk == 0) ? 0u : 1u);
     }
 };
 
@@ -988,6 +1018,7 @@ GRPO_TC_KERNEL(grpo_fwd_lse_kernel, FwdT)
     }
 
 GRPO_PAIR_KERNEL(grpo_fwd_pair_kernel, FwdPairT)
+GRPO_PAIR_KERNEL(grpo_fwd_pair_e4m3_kernel, FwdPairF8T)
 GRPO_PAIR_KERNEL(grpo_dh_pair_kernel, DhPairT)
 GRPO_PAIR_KERNEL(grpo_dw_pair_kernel, DwPairT)
 #undef GRPO_PAIR_KERNEL
@@ -1027,6 +1058,11 @@ cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CU
                             const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st) {
     return bf16 ? launch_tc<FwdPairT, 2>(grpo_fwd_pair_kernel<true>, p, mHp, mHr, mW, n_sm, st)
                 : launch_tc<FwdPairT, 2>(grpo_fwd_pair_kernel<false>, p, mHp, mHr, mW, n_sm, st);
+}
+
+cudaError_t launch_fwd_pair_e4m3(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
+                                 const CUtensorMap& mW, int n_sm, cudaStream_t st) {
+    return launch_tc<FwdPairF8T, 2>(grpo_fwd_pair_e4m3_kernel<true>, p, mHp, mHr, mW, n_sm, st);
 }
 
 cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm, bool bf16,

@@ -54,6 +54,7 @@ def _L():
         lib.synth_permutation.argtypes = [u64, u64, ctypes.c_int32, p]
         lib.synth_to_bf16.argtypes = [p, i64, p]
         lib.synth_to_f16.argtypes = [p, i64, p]
+        lib.synth_to_e4m3.argtypes = [p, i64, ctypes.c_float, p]
         _lib = lib
     return _lib
 
@@ -105,6 +106,23 @@ def to_f16_bits(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, np.float32)
     out = np.empty(x.shape, np.uint16)
     _L().synth_to_f16(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+E4M3_MAX = 448.0
+
+
+def e4m3_scale(x: np.ndarray) -> float:
+    """Per-tensor scale that maps max|x| onto the largest finite e4m3 value."""
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    return float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+
+
+def to_e4m3_bits(x: np.ndarray, scale: float) -> np.ndarray:
+    """fp32 values x -> e4m3 codes of x / scale (round to nearest even, saturating)."""
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _L().synth_to_e4m3(_ptr(x), x.size, scale, _ptr(out))
     return out
 
 
@@ -183,6 +201,24 @@ def lengths_for(cfg: Config, seed: int = 0) -> np.ndarray:
 def rewards_for(cfg: Config, seed: int = 0) -> np.ndarray:
     b = bits(seed, S_RBIT, cfg.n_seq).astype(np.float32)
     return (b + normal_f32(seed, S_RNOISE, cfg.n_seq, 0.1)).astype(np.float32)
+
+
+def generate_e4m3(cfg: Config, seed: int = 0) -> Workload:
+    """The workload of `generate` quantised to e4m3 with one scale per tensor.
+
+    h_pol / h_ref / W hold e4m3 codes (uint8); extra["scales"] = (s_pol, s_ref, s_w)
+    with value = decode(code) * scale.  The reference rows are formed from the
+    unrounded policy rows, as in `generate`."""
+    N, d, V = cfg.N, cfg.d, cfg.V
+    h32 = normal_f32(seed, S_HPOL, N * d, 1.0)
+    r32 = normal_f32(seed, S_REFNOISE, N * d, cfg.sigma_ref, base=h32)
+    w32 = normal_f32(seed, S_W, V * d, cfg.w_sigma)
+    s_pol, s_ref, s_w = e4m3_scale(h32), e4m3_scale(r32), e4m3_scale(w32)
+    wl = Workload(cfg, to_e4m3_bits(h32, s_pol).reshape(N, d), to_e4m3_bits(r32, s_ref).reshape(N, d),
+                  to_e4m3_bits(w32, s_w).reshape(V, d), uniform_int(seed, S_TOK, N, 0, V - 1),
+                  lengths_for(cfg, seed), rewards_for(cfg, seed))
+    wl.extra["scales"] = (s_pol, s_ref, s_w)
+    return wl
 
 
 def generate(cfg: Config, seed: int = 0, with_w: bool = True) -> Workload:

@@ -135,3 +135,45 @@ void synth_to_f16(const float* in, int64_t n, uint16_t* out) {
         out[i] = h;
     }
 }
+
+/* fp32 -> OCP FP8 E4M3 bit pattern of x / scale: round to nearest even,
+ * saturating to +-448 (the format has no infinities; 0x7F / 0xFF are NaN). */
+static uint8_t f32_to_e4m3(float xf) {
+    double x = (double)xf;
+    uint8_t sign = 0;
+    if (x < 0) { sign = 0x80; x = -x; }
+    if (x >= 448.0) return (uint8_t)(sign | 0x7E);
+    if (x < ldexp(1.0, -10)) {                            /* below half the smallest subnormal */
+        return sign;
+    }
+    int e;
+    double m = frexp(x, &e);                              /* x = m * 2^e, m in [0.5, 1) */
+    int exp_unbiased = e - 1;                             /* x = 1.f * 2^(e-1) */
+    uint32_t code;
+    if (exp_unbiased < -6) {                              /* subnormal: units of 2^-9 */
+        double q = x / ldexp(1.0, -9);
+        double fl = floor(q);
+        double r = q - fl;
+        uint32_t n = (uint32_t)fl;
+        if (r > 0.5 || (r == 0.5 && (n & 1u))) n += 1;
+        code = n;                                         /* n == 8 rolls into the smallest normal */
+    } else {
+        double frac = m * 2.0 - 1.0;                      /* in [0, 1) */
+        double q = frac * 8.0;
+        double fl = floor(q);
+        double r = q - fl;
+        uint32_t mant = (uint32_t)fl;
+        if (r > 0.5 || (r == 0.5 && (mant & 1u))) mant += 1;
+        uint32_t be = (uint32_t)(exp_unbiased + 7);
+        if (mant == 8) { mant = 0; be += 1; }
+        code = (be << 3) | mant;
+        if (code > 0x7E) code = 0x7E;
+    }
+    return (uint8_t)(sign | code);
+}
+
+void synth_to_e4m3(const float* in, int64_t n, float scale, uint8_t* out) {
+    const float inv = 1.0f / scale;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e4m3(in[i] * inv);
+}

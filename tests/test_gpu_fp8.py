@@ -1,0 +1,89 @@
+"""The E4M3 forward (grpo_loss_fwd_fp8) against the fp64 oracle on the same
+8-bit inputs: the oracle reads every code times its tensor's scale exactly in
+fp64, so this is the same parity bar as the 16-bit forward."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import rl_fine_tuning_gb300 as rg  # noqa: E402
+from test_gpu_parity import assert_fwd_parity  # noqa: E402
+
+
+def run_fp8(wl8, mask=None, eval_rows=None):
+    cfg = wl8.cfg
+    s_pol, s_ref, s_w = wl8.extra["scales"]
+    shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.E4M3, beta=cfg.beta, eps=cfg.eps)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    h_pol, h_ref, W = dev(wl8.h_pol), dev(wl8.h_ref), dev(wl8.W)
+    tokens, lengths, rewards = dev(wl8.tokens), dev(wl8.lengths), dev(wl8.rewards)
+    adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
+    rg.grpo_group_advantages(rewards, cfg.n_groups, cfg.G, cfg.eps, True, adv)
+    if mask is None:
+        m = torch.empty(cfg.N, dtype=torch.uint8, device="cuda")
+        rg.grpo_build_mask(lengths, shape, m)
+    else:
+        m = dev(mask.astype(np.uint8))
+    ws = torch.empty(rg.grpo_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    stats = torch.zeros((cfg.N, 5), dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rg.grpo_loss_fwd_fp8(h_pol, h_ref, W, s_pol, s_ref, s_w, tokens, m, adv, shape, ws, loss, stats, status)
+    torch.cuda.synchronize()
+    res = dict(loss=float(loss.item()), status=int(status.item()), row_stats=stats.cpu().numpy().astype(np.float64),
+               adv=adv.cpu().numpy(), mask=m.cpu().numpy())
+    exp = oracle.expected(oracle.dequantized_workload(wl8), mask=res["mask"], eval_rows=eval_rows,
+                          want_dH=False, want_dW=False)
+    return res, exp
+
+
+@pytest.mark.parametrize("over", [dict(), dict(G=4, L=500, d=384, V=3000, len_lo=1, len_hi=500),
+                                  dict(G=2, L=300, d=256, V=777, sigma_ref=0.4)])
+def test_fp8_forward_parity(over):
+    cfg = synth.make_config("tiny", **over)
+    res, exp = run_fp8(synth.generate_e4m3(cfg, seed=41))
+    assert np.array_equal(res["adv"].view(np.uint32), exp["adv"].view(np.uint32))
+    assert_fwd_parity(res, exp)
+
+
+def test_fp8_rejects_bad_arguments():
+    cfg = synth.make_config("tiny", d=192)
+    wl8 = synth.generate_e4m3(synth.make_config("tiny"), seed=1)
+    with pytest.raises(rg.GrpoError) as e:            # d not a multiple of 128
+        shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, 192, cfg.V, rg.E4M3)
+        t = torch.zeros(16, dtype=torch.int32, device="cuda")
+        rg.grpo_loss_fwd_fp8(t, t, t, 1.0, 1.0, 1.0, t, t, t, shape, torch.zeros(64, dtype=torch.uint8, device="cuda"),
+                             t, None, t)
+    assert e.value.code == 2
+    with pytest.raises(rg.GrpoError) as e:            # 16-bit shape handed to the 8-bit entry point
+        shape = rg.make_shape(1, 4, 64, 128, 1024, rg.BF16)
+        t = torch.zeros(16, dtype=torch.int32, device="cuda")
+        rg.grpo_loss_fwd_fp8(t, t, t, 1.0, 1.0, 1.0, t, t, t, shape, torch.zeros(64, dtype=torch.uint8, device="cuda"),
+                             t, None, t)
+    assert e.value.code == 5
+    del wl8
+
+
+def test_fp8_forward_full_size_sampled_rows():
+    cfg = synth.CONFIGS["llama-3.1-8b-head"]
+    wl8 = synth.generate_e4m3(cfg, seed=0)
+    mask = oracle.build_mask(wl8.lengths, cfg.L)
+    rows = oracle.valid_rows(mask)
+    rng = np.random.default_rng(5)
+    sample = np.sort(rng.choice(rows, size=12, replace=False)).astype(np.int32)
+    res, exp = run_fp8(wl8, eval_rows=sample)
+    assert res["status"] == 0
+    rs = res["row_stats"][sample]
+    for col, key in ((0, "lse_pol"), (1, "lse_ref"), (2, "q"), (3, "p")):
+        ref = exp["terms"][key]
+        assert np.all(np.abs(rs[:, col] - ref) <= 1e-3 * np.maximum(1.0, np.abs(ref))), key
+    A = exp["adv"][rows // cfg.L].astype(np.float64)
+    ell = -A + cfg.beta * res["row_stats"][rows, 4]
+    assert abs(res["loss"] - ell.mean()) <= 1e-5 * max(1e-3, abs(ell.mean()))

@@ -86,6 +86,40 @@ def test_generator_rounding_matches_libraries():
     assert np.array_equal(synth.to_bf16_bits(x), tb)
 
 
+def test_e4m3_decoding_special_values():
+    """OCP FP8 E4M3: bias 7, 3 mantissa bits, no infinities, S.1111.111 = NaN."""
+    lib = oracle._L()
+    dec = np.array([lib.oracle_e4m3_to_f64(i) for i in range(256)])
+    assert dec[0x38] == 1.0 and dec[0x7E] == 448.0 and dec[0x08] == 2.0 ** -6 and dec[0x01] == 2.0 ** -9
+    assert dec[0x07] == 7 * 2.0 ** -9 and dec[0x40] == 2.0 and dec[0x3C] == 1.5
+    assert np.isnan(dec[0x7F]) and np.isnan(dec[0xFF])
+    assert dec[0x00] == 0.0 and dec[0x80] == 0.0 and np.signbit(dec[0x80])
+    assert np.array_equal(dec[0x80:0xFF], -dec[0x00:0x7F])
+    assert np.all(np.diff(dec[0x00:0x7F]) > 0)                 # codes are ordered like their values
+
+
+def test_generator_e4m3_rounding_brute_force():
+    """Each code is the nearest e4m3 value to x/scale (ties to an even mantissa), saturating at 448."""
+    lib = oracle._L()
+    dec = np.array([lib.oracle_e4m3_to_f64(i) for i in range(256)])
+    pos = np.arange(0x7F)                                       # finite non-negative codes
+    rng = np.random.default_rng(3)
+    x = np.concatenate([rng.normal(0, 40, 4000), rng.uniform(-500, 500, 2000), rng.normal(0, 1e-2, 2000),
+                        dec[pos] + 0.5 * np.diff(np.append(dec[pos], 480.0))])     # exact midpoints
+    x = x.astype(np.float32)
+    codes = synth.to_e4m3_bits(x, 1.0)
+    for xi, c in zip(x.astype(np.float64), codes):
+        a = abs(xi)
+        err = np.abs(dec[pos] - min(a, 448.0))
+        best = pos[err == err.min()]
+        if best.size > 1:
+            best = best[(best & 1) == 0]
+        assert (c & 0x7F) == best[0], (xi, hex(c), hex(best[0]))
+        assert (c >> 7) == (1 if (xi < 0 and (c & 0x7F) != 0) else (c >> 7))
+    s = synth.e4m3_scale(x)
+    assert np.max(np.abs(oracle.e4m3_values(synth.to_e4m3_bits(x, s), s))) <= 448.0 * s * (1 + 1e-7)
+
+
 def test_generator_is_counter_based():
     a = synth.normal_f32(0, 1, 1000)
     b = synth.normal_f32(0, 1, 500, offset=500)
