@@ -236,6 +236,14 @@ int grpo_profile_enable(int on);
 int grpo_profile_collect(double* ms, long long* launches, int n_kinds);
 unsigned long long grpo_kernel_launches(void);
 
+/* Self-test of the bounded device waits: one CTA waits, with the wait the
+ * kernels use, on an mbarrier that nothing completes.  It gives up after about
+ * a second and writes GRPO_ERR_TIMEOUT to *status (device int32, set to 0 by
+ * the caller beforehand) and the nanoseconds it waited to *waited_ns (device
+ * uint64).  The context stays usable.  The pages have no counterpart; it
+ * checks the library's own guarantee that no kernel waits forever. */
+int grpo_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns, grpo_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* grpo_status_string(int status);
 

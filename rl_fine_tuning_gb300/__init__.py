@@ -217,3 +217,11 @@ def grpo_loss_fwd_fp8(h_pol, h_ref, W, scale_h_pol, scale_h_ref, scale_w, tokens
     _check(fn(_ptr(h_pol), _ptr(h_ref), _ptr(W), float(scale_h_pol), float(scale_h_ref), float(scale_w), _ptr(tokens),
               _ptr(mask), _ptr(adv), ctypes.byref(shape), _ptr(workspace), _nbytes(workspace), _ptr(loss_out),
               _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_fp8")
+
+
+def grpo_selftest_wait_timeout(status, waited_ns, stream=None):
+    fn = load().grpo_selftest_wait_timeout
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    _check(fn(_ptr(status), _ptr(waited_ns), _stream(stream)), "grpo_selftest_wait_timeout")

@@ -593,6 +593,16 @@ int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float
     return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr, &f8);
 }
 
+int grpo_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns, grpo_stream_t stream) {
+    if (!status || !waited_ns || !aligned(status, 4) || !aligned(waited_ns, 8)) return GRPO_ERR_POINTER;
+    DeviceInfo dev;
+    const int rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    return launch_wait_selftest(status, waited_ns, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_LAUNCH;
+}
+
 const char* grpo_status_string(int status) {
     switch (status) {
         case GRPO_OK: return "ok";

@@ -131,6 +131,7 @@ cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, cudaStream_
 cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, cudaStream_t st);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st);
 
+cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cudaStream_t st);
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
                        const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
 // CTA-pair (M=256) variants: forward of a chunk, dH, dW

@@ -995,6 +995,33 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
     }
 }
 
+// ====================================================================== wait self-test
+// One CTA waits on an mbarrier that nothing ever completes, through the same
+// bounded wait the kernels use: it must give up after kWaitTimeoutNs and
+// report GRPO_ERR_TIMEOUT instead of hanging.
+__global__ void __launch_bounds__(32) k_wait_selftest(int* status, unsigned long long* waited_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const uint64_t t0 = globaltimer();
+    const bool done = mbar_wait(&bar, 0, &abort_flag, status);
+    const uint64_t t1 = globaltimer();
+    if (threadIdx.x == 0) {
+        *waited_ns = t1 - t0;
+        if (done) atomicCAS(status, 0, -1);   // the phase cannot have completed
+    }
+}
+
+cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cudaStream_t st) {
+    k_wait_selftest<<<1, 32, 0, st>>>(status, waited_ns);
+    return cudaGetLastError();
+}
+
 // ====================================================================== launches
 
 // One named kernel per traits class (the names show up in profiles).

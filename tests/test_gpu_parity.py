@@ -267,3 +267,16 @@ def test_host_validation_errors():
         rg.grpo_loss_fwd(dw.h_pol.data_ptr() + 2, dw.h_ref, dw.W, dw.tokens, dw.mask, dw.adv, dw.shape, dw.ws,
                          dw.loss, None, dw.status)
     assert e.value.code == 1
+
+
+def test_bounded_wait_times_out_and_context_stays_usable():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    waited = torch.zeros(1, dtype=torch.int64, device="cuda")
+    rg.grpo_selftest_wait_timeout(status, waited)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 6                      # GRPO_ERR_TIMEOUT
+    assert 0.9e9 <= int(waited.item()) <= 5e9           # about one second, then it gave up
+    # the context still runs the real path
+    _, _, res, exp = _run(synth.CONFIGS["tiny"])
+    assert_fwd_parity(res, exp)
+    assert_grad_parity(res, exp)
