@@ -498,23 +498,32 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
 // tile, so per SM a K-stage is 32 KB of shared memory instead of 48-64 KB, and
 // its tensor memory holds a double-buffered 128x256 accumulator.
 
-// 128-row tiles of a chunk visited group by group: all splits of a group of
-// kFwdGroup tiles run together, so W streams from L2 once per group.
-constexpr int kFwdGroup = 8;
+// Work-unit orders.  A unit is a pair (a, b); the a-indices are visited in
+// groups of G: all b of a group run before the next group starts, and within a
+// group the a-indices are fastest.  With G = 1 the b-index is fastest.  The
+// group sizes were chosen by timing on GB300 (16 row tiles per group for the
+// chunk forward: each W tile is then shared in L2 by 16 tiles).
+constexpr int kFwdGroup = 16;   // chunk forward: a = 128-row tile, b = vocabulary split
+constexpr int kDhGroup = 1;     // dH: a = pair of 128-row tiles, b = 256-wide d tile
+constexpr int kDwGroup = 1;     // dW: a = pair of 128-row vocabulary tiles, b = 256-wide d tile
+
+__device__ __forceinline__ void decode_grouped(int unit, int n_a, int n_b, int G, int* a, int* b) {
+    const int full = (n_a / G) * G;
+    if (unit < full * n_b) {
+        const int gi = unit / (G * n_b);
+        const int r = unit - gi * G * n_b;
+        *b = r / G;
+        *a = gi * G + (r - *b * G);
+    } else {
+        const int u2 = unit - full * n_b;
+        const int g_last = n_a - full;
+        *b = u2 / g_last;
+        *a = full + (u2 - *b * g_last);
+    }
+}
 
 __device__ __forceinline__ void decode_tile_split(int unit, int n_mt, int S, int* mt, int* split) {
-    const int full = (n_mt / kFwdGroup) * kFwdGroup;
-    if (unit < full * S) {
-        const int gi = unit / (kFwdGroup * S);
-        const int r = unit - gi * kFwdGroup * S;
-        *split = r / kFwdGroup;
-        *mt = gi * kFwdGroup + (r - *split * kFwdGroup);
-    } else {
-        const int u2 = unit - full * S;
-        const int g_last = n_mt - full;
-        *split = u2 / g_last;
-        *mt = full + (u2 - *split * g_last);
-    }
+    decode_grouped(unit, n_mt, S, kFwdGroup, mt, split);
 }
 
 // Forward of one chunk: the leader's A rows are the policy tile, the peer's the
@@ -684,7 +693,7 @@ struct DhPairT {
     struct Epi {
         int unused;
     };
-    // unit = m-pair * n_nt + d-tile; the CTA of rank r takes m-tile 2*pair + r
+    // unit -> (pair of 128-row tiles, d tile); the CTA of rank r takes m-tile 2*pair + r
     __device__ static bool setup(const Params& p, Sched& sc) {
         if (!chunk_setup(p, sc, 2)) return false;
         sc.n_nt = (p.d + kBN - 1) / kBN;
@@ -693,11 +702,23 @@ struct DhPairT {
         sc.n_units = sc.n_g * sc.n_nt;
         return true;
     }
-    __device__ static int mtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * 2 + rank; }
+    __device__ static void decode(const Sched& sc, int unit, int* pair, int* dt) {
+        decode_grouped(unit, sc.n_g, sc.n_nt, kDhGroup, pair, dt);
+    }
+    __device__ static int mtile(const Sched& sc, int unit, int rank) {
+        int pair, dt;
+        decode(sc, unit, &pair, &dt);
+        return pair * 2 + rank;
+    }
+    __device__ static int dtile(const Sched& sc, int unit) {
+        int pair, dt;
+        decode(sc, unit, &pair, &dt);
+        return dt;
+    }
     __device__ static int items(const Params&, const Sched&, int) { return 1; }
     __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
     __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
-        return Coord{mtile(sc, unit, rank) * kBM, (unit % sc.n_nt) * kBN};
+        return Coord{mtile(sc, unit, rank) * kBM, dtile(sc, unit) * kBN};
     }
     __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
         return 2 * 16384 + 8192 * min(4, (p.d - c.n0) / 64);
@@ -724,7 +745,7 @@ struct DhPairT {
     __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
         const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
         const int slot = mtile(sc, unit, rank) * kBM + row;
-        const int n0 = (unit % sc.n_nt) * kBN;
+        const int n0 = dtile(sc, unit) * kBN;
         const bool valid = slot < sc.n_c;
         if (!__any_sync(0xffffffffu, valid)) return;
         const int t = valid ? p.rows[sc.c0 + slot] : 0;
@@ -765,7 +786,7 @@ struct DwPairT {
     struct Epi {
         int unused;
     };
-    // unit = vocab-pair * n_nt + d-tile; the CTA of rank r takes vocabulary tile 2*pair + r
+    // unit -> (pair of vocabulary tiles, d tile); the CTA of rank r takes vocabulary tile 2*pair + r
     __device__ static bool setup(const Params& p, Sched& sc) {
         if (!chunk_setup(p, sc, 2)) return false;
         sc.n_nt = (p.d + kBN - 1) / kBN;
@@ -774,11 +795,23 @@ struct DwPairT {
         sc.n_units = sc.n_g * sc.n_nt;
         return true;
     }
-    __device__ static int vtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * 2 + rank; }
+    __device__ static void decode(const Sched& sc, int unit, int* pair, int* dt) {
+        decode_grouped(unit, sc.n_g, sc.n_nt, kDwGroup, pair, dt);
+    }
+    __device__ static int vtile(const Sched& sc, int unit, int rank) {
+        int pair, dt;
+        decode(sc, unit, &pair, &dt);
+        return pair * 2 + rank;
+    }
+    __device__ static int dtile(const Sched& sc, int unit) {
+        int pair, dt;
+        decode(sc, unit, &pair, &dt);
+        return dt;
+    }
     __device__ static int items(const Params&, const Sched&, int) { return 1; }
     __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
     __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
-        return Coord{vtile(sc, unit, rank) * kBM, (unit % sc.n_nt) * kBN};
+        return Coord{vtile(sc, unit, rank) * kBM, dtile(sc, unit) * kBN};
     }
     __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
         return 2 * 16384 + 8192 * min(4, (p.d - c.n0) / 64);
@@ -806,7 +839,7 @@ struct DwPairT {
     __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
         const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
         const int v = vtile(sc, unit, rank) * kBM + row;
-        const int n0 = (unit % sc.n_nt) * kBN;
+        const int n0 = dtile(sc, unit) * kBN;
         const bool valid = v < p.V;
         if (!__any_sync(0xffffffffu, valid)) return;
         const bool first_chunk = p.chunk == 0;
