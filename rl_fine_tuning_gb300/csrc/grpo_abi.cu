@@ -164,13 +164,35 @@ static void split_vocab(int n_ntiles, int max_splits, int* S, int* nps) {
     *S = (n_ntiles + *nps - 1) / *nps;
 }
 
+// Splits of the chunk forward.  Its static schedule hands every CTA pair the
+// same number of (row tile, split) units when a chunk has one row tile per
+// pair, so splits of one size give every pair the same work.  Prefer the
+// equal division of the vocabulary tiles whose split count is closest to
+// `target` within [target/2, max_splits]; without one, fall back to ranges of
+// at most `target` splits with a shorter last range.
+static void split_vocab_even(int n_ntiles, int target, int max_splits, int* S, int* nps) {
+    int best = 0;
+    for (int s = target / 2; s <= max_splits && s <= n_ntiles; ++s) {
+        if (n_ntiles % s != 0) continue;
+        const int dist = s > target ? s - target : target - s;
+        const int bdist = best > target ? best - target : target - best;
+        if (best == 0 || dist < bdist) best = s;
+    }
+    if (best == 0) {
+        split_vocab(n_ntiles, target, S, nps);
+        return;
+    }
+    *S = best;
+    *nps = n_ntiles / best;
+}
+
 bool ws_layout(const grpo_shape& s, WsLayout* o) {
     if (!shape_ok(s)) return false;
     const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
     o->N = N;
     o->n_ntiles = (s.V + kBN - 1) / kBN;
     split_vocab(o->n_ntiles, kTileSplits, &o->S, &o->nps);
-    split_vocab(o->n_ntiles, kChunkSplits, &o->Sc, &o->npsc);
+    split_vocab_even(o->n_ntiles, kChunkSplits, kChunkSplitsMax, &o->Sc, &o->npsc);
     o->R = chunk_rows_of(s);
     o->V_pad = (s.V + 63) / 64 * 64;
     o->nc32 = (s.V + 31) / 32;

@@ -13,7 +13,8 @@ constexpr int kBM = 128;              // rows (or vocabulary rows for dW) per MM
 constexpr int kBK = 64;               // K elements per pipeline stage: one 128-byte swizzle span
 constexpr int kBN = 256;              // accumulator columns per MMA tile
 constexpr int kTileSplits = 8;        // vocabulary splits of a forward row tile (forward-only path)
-constexpr int kChunkSplits = 64;      // vocabulary splits of a chunk row tile (forward+backward path)
+constexpr int kChunkSplits = 64;      // vocabulary splits of a chunk row tile (forward+backward path), target
+constexpr int kChunkSplitsMax = 256;  // ... and the most it may take to divide the vocabulary tiles evenly
 // Default rows per backward chunk: 76 tiles of 128.  On 152 SMs (76 CTA pairs)
 // the chunk's forward units (76 tiles x 64 splits) and its dH units (38 tile
 // pairs x d/256 tiles, for d = 1536, 4096 or 5120) divide evenly over the pairs.
