@@ -155,9 +155,12 @@ int grpo_loss_fwd(const void* h_pol, const void* h_ref, const void* W, const int
  *               scale otherwise -- "Long-context GRPO", section 3: mixed
  *               precision with automatic loss scaling breaks a naive linear
  *               cross entropy unless handled)
- *   dH [N x d] (dtype; device, written): loss_scale * d loss / d h_pol;
- *               exactly 0 on masked rows
- *   dW [V x d] fp32 (device, overwritten): loss_scale * d loss / d W
+ *   dH [N x d] (dtype; device, written, 32-byte aligned): loss_scale *
+ *               d loss / d h_pol; exactly 0 on masked rows
+ *   dW [V x d] fp32 (device, overwritten, 32-byte aligned): loss_scale *
+ *               d loss / d W
+ *   (the gradient epilogues write whole 32-byte sectors; a dH or dW that is
+ *   only 16-byte aligned is refused with GRPO_ERR_POINTER)
  *   found_inf: one int32 (device) <- 1 if any scaled gradient value (the
  *               16-bit dlogits, dH or dW) is not finite, else 0.  The caller
  *               lowers the scale and calls again when it is set.

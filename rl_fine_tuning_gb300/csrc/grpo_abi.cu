@@ -195,7 +195,7 @@ bool ws_layout(const grpo_shape& s, WsLayout* o) {
     split_vocab_even(o->n_ntiles, kChunkSplits, kChunkSplitsMax, &o->Sc, &o->npsc);
     o->R = chunk_rows_of(s);
     o->V_pad = (s.V + 63) / 64 * 64;
-    o->nc32 = (s.V + 31) / 32;
+    o->nc32 = ((s.V + 31) / 32 + 7) / 8 * 8;   // whole 32-byte sectors per 256-column tile
     o->nblk = static_cast<int>((N + kMergeThreads - 1) / kMergeThreads);
     o->n_sched = static_cast<int>(2 + (N + o->R - 1) / o->R);
     o->n_seq = s.n_groups * s.G;
@@ -581,7 +581,7 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     WsLayout L;
     int rc = validate(in, &L);
     if (rc != GRPO_OK) return rc;
-    if (!dH || !dW || !found_inf || !aligned(dH, 16) || !aligned(dW, 16) || !aligned(found_inf, 4))
+    if (!dH || !dW || !found_inf || !aligned(dH, 32) || !aligned(dW, 32) || !aligned(found_inf, 4))
         return GRPO_ERR_POINTER;
     if (!(loss_scale > 0.f) || !std::isfinite(loss_scale)) return GRPO_ERR_SHAPE;
     DeviceInfo dev;

@@ -43,7 +43,7 @@ struct WsLayout {
     int n_ntiles;    // ceil(V / kBN)
     int R;           // rows per backward chunk (buffer height)
     int V_pad;       // row pitch of the dlogits buffer, elements
-    int nc32;        // 32-column groups per vocabulary row
+    int nc32;        // row pitch of the running maxima: 32-column groups per vocabulary row, rounded up to 8
     int nblk;        // loss-reduction blocks
     int n_sched;     // scheduler counters
     int n_seq;       // completions (n_groups * G)

@@ -601,6 +601,10 @@ struct FwdPairT {
         const bool keep = rank == 0 && p.E != nullptr && e.valid;
         uint16_t* erow = keep ? p.E + static_cast<int64_t>(e.slot) * p.V_pad : nullptr;
         float* mrow = keep ? p.mx + static_cast<int64_t>(e.slot) * p.nc32 : nullptr;
+        // running maxima of the tile's eight 32-column groups, stored together at the end
+        float mv[kBN / 32];
+#pragma unroll
+        for (int j = 0; j < kBN / 32; ++j) mv[j] = 0.f;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
             const int col0 = n0 + c * 32;
@@ -639,14 +643,25 @@ struct FwdPairT {
             e.s = fmaf(e.s, fast_exp2(fmaf(e.m, kLog2e, -mb)), acc);
             e.m = m_new;
             if (keep) {
-                uint4* o4 = reinterpret_cast<uint4*>(erow + col0);
+                // 64 bytes of one row as two whole 32-byte sectors
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    o4[j] = make_uint4(pack2(v[8 * j], v[8 * j + 1], true), pack2(v[8 * j + 2], v[8 * j + 3], true),
-                                       pack2(v[8 * j + 4], v[8 * j + 5], true), pack2(v[8 * j + 6], v[8 * j + 7], true));
-                mrow[col0 >> 5] = m_new;
+                for (int h = 0; h < 2; ++h)
+                    st_global_v8(erow + col0 + 16 * h, pack2(v[16 * h], v[16 * h + 1], true),
+                                 pack2(v[16 * h + 2], v[16 * h + 3], true), pack2(v[16 * h + 4], v[16 * h + 5], true),
+                                 pack2(v[16 * h + 6], v[16 * h + 7], true), pack2(v[16 * h + 8], v[16 * h + 9], true),
+                                 pack2(v[16 * h + 10], v[16 * h + 11], true),
+                                 pack2(v[16 * h + 12], v[16 * h + 13], true),
+                                 pack2(v[16 * h + 14], v[16 * h + 15], true));
+#pragma unroll
+                for (int j = 0; j < kBN / 32; ++j)
+                    if (c == j) mv[j] = m_new;
             }
         }
+        // the row pitch of mx is a multiple of 8 groups and n0 of 256 columns: 32-byte aligned
+        if (keep)
+            st_global_v8(mrow + (n0 >> 5), __float_as_uint(mv[0]), __float_as_uint(mv[1]), __float_as_uint(mv[2]),
+                         __float_as_uint(mv[3]), __float_as_uint(mv[4]), __float_as_uint(mv[5]),
+                         __float_as_uint(mv[6]), __float_as_uint(mv[7]));
     }
     // the leader writes the policy half of the partials, the peer the reference half
     __device__ static void epi_end(const Params& p, const Sched&, int rank, Epi& e) {
@@ -765,9 +780,11 @@ struct DhPairT {
                 for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
             }
             if (valid) {
-                uint4* o4 = reinterpret_cast<uint4*>(out + col0);
+                // 64 bytes of one dH row as two whole sectors (dH is 32-byte aligned, d a multiple of 64)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                for (int h = 0; h < 2; ++h)
+                    st_global_v8(out + col0 + 16 * h, pk[8 * h], pk[8 * h + 1], pk[8 * h + 2], pk[8 * h + 3],
+                                 pk[8 * h + 4], pk[8 * h + 5], pk[8 * h + 6], pk[8 * h + 7]);
             }
         }
         if (bad && valid) atomicOr(p.found_inf, 1);
@@ -852,20 +869,24 @@ struct DwPairT {
             float x[32];
             tmem_ld32(tacc + c * 32, x);
             if (valid) {
-                float4* o4 = reinterpret_cast<float4*>(out + col0);
+                // 128 bytes of one dW row as four whole sectors (dW is 32-byte aligned)
+                float* o = out + col0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float4 r = make_float4(x[4 * j] * sc.winv, x[4 * j + 1] * sc.winv, x[4 * j + 2] * sc.winv,
-                                           x[4 * j + 3] * sc.winv);
+                for (int j = 0; j < 4; ++j) {
+                    float r[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) r[i] = x[8 * j + i] * sc.winv;
                     if (!first_chunk) {
-                        const float4 o = o4[j];
-                        r.x += o.x;
-                        r.y += o.y;
-                        r.z += o.z;
-                        r.w += o.w;
+                        float prev[8];
+                        ld_global_v8(o + 8 * j, prev);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) r[i] += prev[i];
                     }
-                    bad |= !(isfinite(r.x) && isfinite(r.y) && isfinite(r.z) && isfinite(r.w));
-                    o4[j] = r;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) bad |= !isfinite(r[i]);
+                    st_global_v8(o + 8 * j, __float_as_uint(r[0]), __float_as_uint(r[1]), __float_as_uint(r[2]),
+                                 __float_as_uint(r[3]), __float_as_uint(r[4]), __float_as_uint(r[5]),
+                                 __float_as_uint(r[6]), __float_as_uint(r[7]));
                 }
             }
         }

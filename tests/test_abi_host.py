@@ -101,6 +101,8 @@ def test_validation_codes_without_a_device(lib):
     assert lib.grpo_group_advantages(None, 1, 4, ctypes.c_float(1e-4), 1, P, None) == 1
     fb = lib.grpo_loss_fwd_bwd
     assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(1.0), P, need, P, None, P, P, None, P, None) == 1
+    assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(1.0), P, need, P, P + 16, P, P, None, P, None) == 1
+    assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(1.0), P, need, P, P, P + 16, P, None, P, None) == 1
     assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(0.0), P, need, P, P, P, P, None, P, None) == 2
     assert fb(P, P, P, P, P, P, ctypes.byref(s), ctypes.c_float(float("nan")), P, need, P, P, P, P, None, P,
               None) == 2
