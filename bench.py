@@ -446,7 +446,7 @@ def run_ours(args, ranks):
 
 def run_forward_modes(args, ranks):
     """Forward-only throughput: grpo_loss_fwd on bf16 inputs and grpo_loss_fwd_fp8 on
-    the same workload quantised to e4m3 (one scale per tensor)."""
+    the same workload quantised to e4m3 and to e5m2 (one scale per tensor)."""
     import numpy as np
     import torch
 
@@ -459,15 +459,16 @@ def run_forward_modes(args, ranks):
     n_valid = int(np.minimum(np.maximum(synth.lengths_for(cfg, 0), 0), cfg.L).sum())
     stream = torch.cuda.current_stream()
     out = {}
-    for mode in ("bf16", "e4m3"):
+    for mode in ("bf16", "e4m3", "e5m2"):
         if mode == "bf16":
             wl = synth.generate(cfg, seed=0)
             mats = [torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16) for a in (wl.h_pol, wl.h_ref, wl.W)]
             shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.BF16, beta=cfg.beta, eps=cfg.eps)
         else:
-            wl = synth.generate_e4m3(cfg, seed=0)
+            wl = synth.generate_fp8(cfg, seed=0, fmt=mode)
             mats = [torch.from_numpy(a).cuda() for a in (wl.h_pol, wl.h_ref, wl.W)]
-            shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.E4M3, beta=cfg.beta, eps=cfg.eps)
+            shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.E4M3 if mode == "e4m3" else rg.E5M2,
+                                  beta=cfg.beta, eps=cfg.eps)
         tokens, lengths, rewards = (torch.from_numpy(a).cuda() for a in (wl.tokens, wl.lengths, wl.rewards))
         adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
         mask = torch.empty(cfg.N, dtype=torch.uint8, device="cuda")
@@ -501,7 +502,7 @@ def run_forward_modes(args, ranks):
         del mats, ws, wl
         torch.cuda.empty_cache()
     pk, pk_kind = peaks()
-    line = {"metric": "GRPO loss forward tokens/s (bf16 and e4m3 inputs)", "value": out["e4m3"]["tokens_per_s"],
+    line = {"metric": "GRPO loss forward tokens/s (bf16, e4m3 and e5m2 inputs)", "value": out["e4m3"]["tokens_per_s"],
             "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": out["e4m3"]["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": cfg_dict(cfg, {"n_valid": n_valid}),

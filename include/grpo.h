@@ -57,7 +57,7 @@ enum {
     GRPO_ERR_DEVICE = 7      /* device is not sm_103 / lacks the needed shared memory */
 };
 
-typedef enum { GRPO_BF16 = 0, GRPO_FP16 = 1, GRPO_E4M3 = 2 } grpo_dtype;
+typedef enum { GRPO_BF16 = 0, GRPO_FP16 = 1, GRPO_E4M3 = 2, GRPO_E5M2 = 3 } grpo_dtype;
 
 typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
 
@@ -67,7 +67,7 @@ typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
  *   d           : hidden size, a multiple of 64
  *   V           : vocabulary size (>= 1)
  *   dtype       : storage/compute type of h_pol, h_ref, W (and of dH);
- *                 GRPO_E4M3 only with grpo_loss_fwd_fp8
+ *                 GRPO_E4M3 / GRPO_E5M2 only with grpo_loss_fwd_fp8
  *   beta        : KL coefficient (0.04 in the pages' setting)
  *   eps         : added to the group std in grpo_group_advantages
  *   std_unbiased: 1 -> group std with divisor G-1, 0 -> divisor G
@@ -174,13 +174,14 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
                       int32_t* status, grpo_stream_t stream);
 
 /* Forward pass on 8-bit inputs ("Long-context GRPO", section 3: linear cross
- * entropy under float8 mixed precision).  h_pol, h_ref and W hold OCP FP8 E4M3
- * codes (one byte per element, same row-major layouts); element values are
- * code * scale with one scale per tensor (scale_h_pol, scale_h_ref, scale_w
- * > 0).  The logits come from E4M3 tensor-core products accumulated in fp32
- * and multiplied by scale_h * scale_w; everything after that is as in
- * grpo_loss_fwd.  shape->dtype must be GRPO_E4M3 and d a multiple of 128; the
- * workspace is grpo_workspace_bytes(shape).  Forward only: dlogits in e4m3 or
+ * entropy under float8 mixed precision).  h_pol, h_ref and W hold OCP FP8
+ * codes of one format, shape->dtype: GRPO_E4M3 (4 exponent bits, 3 mantissa
+ * bits) or GRPO_E5M2 (5 and 2), one byte per element, same row-major layouts;
+ * element values are code * scale with one scale per tensor (scale_h_pol,
+ * scale_h_ref, scale_w > 0).  The logits come from 8-bit tensor-core products
+ * accumulated in fp32 and multiplied by scale_h * scale_w; everything after
+ * that is as in grpo_loss_fwd.  d must be a multiple of 128; the workspace is
+ * grpo_workspace_bytes(shape).  Forward only: dlogits in e4m3 or
  * e5m2 would carry 6-12% error on the sampled token's entry, far above the
  * gradient tolerance, so the backward stays 16-bit. */
 int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float scale_h_pol, float scale_h_ref,

@@ -52,6 +52,8 @@ def _L():
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
         lib.oracle_e4m3_to_f64.restype = f64
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e5m2_to_f64.restype = f64
+        lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_group_advantages.argtypes = [p, i32, i32, ctypes.c_float, i32, p]
         lib.oracle_build_mask.argtypes = [p, i32, i32, p]
         lib.oracle_valid_rows.restype = i64
@@ -93,20 +95,27 @@ def _mat(a, dtype):
     return np.ascontiguousarray(a, np.uint16)
 
 
-def e4m3_values(codes, scale):
-    """e4m3 codes -> float64 values code * scale (exact in fp64), via the oracle's decoder."""
-    lut = np.array([_L().oracle_e4m3_to_f64(i) for i in range(256)], np.float64)
+def fp8_values(codes, scale, fmt="e4m3"):
+    """OCP FP8 codes ("e4m3" / "e5m2") -> float64 values code * scale (exact in
+    fp64), via the oracle's decoders."""
+    dec = {"e4m3": _L().oracle_e4m3_to_f64, "e5m2": _L().oracle_e5m2_to_f64}[fmt]
+    lut = np.array([dec(i) for i in range(256)], np.float64)
     return lut[np.ascontiguousarray(codes, np.uint8)] * float(scale)
 
 
+def e4m3_values(codes, scale):
+    return fp8_values(codes, scale, "e4m3")
+
+
 def dequantized_workload(wl):
-    """A copy of an e4m3 workload whose matrices are the exact float64 values."""
+    """A copy of an 8-bit workload whose matrices are the exact float64 values."""
     from copy import copy
     s_pol, s_ref, s_w = wl.extra["scales"]
+    fmt = wl.extra.get("fp8", "e4m3")
     out = copy(wl)
-    out.h_pol = e4m3_values(wl.h_pol, s_pol)
-    out.h_ref = e4m3_values(wl.h_ref, s_ref)
-    out.W = e4m3_values(wl.W, s_w)
+    out.h_pol = fp8_values(wl.h_pol, s_pol, fmt)
+    out.h_ref = fp8_values(wl.h_ref, s_ref, fmt)
+    out.W = fp8_values(wl.W, s_w, fmt)
     return out
 
 

@@ -92,6 +92,20 @@ double oracle_e4m3_to_f64(uint8_t b) {
     return sign ? -v : v;
 }
 
+/* OCP FP8 E5M2: 1 sign, 5 exponent bits (bias 15), 2 mantissa bits; exponent
+ * field 31 holds the infinities (mantissa 0) and NaNs; largest finite 57344,
+ * smallest normal 2^-14, smallest subnormal 2^-16. */
+double oracle_e5m2_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 31;
+    int m = b & 3;
+    double v;
+    if (e == 31) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m, -16);
+    else v = ldexp((double)(4 + m), e - 17);
+    return sign ? -v : v;
+}
+
 static inline double ld(const void* p, int type, size_t i) {
     if (type == OR_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[i]);
     if (type == OR_F16) return oracle_f16_to_f64(((const uint16_t*)p)[i]);

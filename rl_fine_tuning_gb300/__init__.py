@@ -24,7 +24,7 @@ __all__ = [
 # kernel kinds of the diagnostics interface, in the order of the GRPO_PROF_* enum
 PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "dlogits", "dh", "dw")
 
-BF16, FP16, E4M3 = 0, 1, 2
+BF16, FP16, E4M3, E5M2 = 0, 1, 2, 3
 TOKEN_MEAN, SEQUENCE_MEAN = 0, 1
 OBJECTIVES = {"grpo": 0, "no_detach": 1, "reverse_kl_q": 2, "forward_kl": 3}
 

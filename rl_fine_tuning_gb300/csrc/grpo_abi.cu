@@ -131,7 +131,7 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t cols, uint64
     return r == CUDA_SUCCESS;
 }
 
-// 2-D row-major matrix of 8-bit elements (E4M3 codes), 128-byte swizzled boxes
+// 2-D row-major matrix of 8-bit elements (FP8 codes), 128-byte swizzled boxes
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch, uint32_t box_cols,
                  uint32_t box_rows) {
     auto fn = encode_fn();
@@ -373,13 +373,14 @@ struct Backward {
     int32_t* found_inf;
 };
 
-// per-tensor scales of E4M3 inputs (forward only)
-struct E4m3Scales {
+// 8-bit inputs (forward only): the format and the per-tensor scales
+struct Fp8Inputs {
+    bool e5m2;
     float h_pol, h_ref, w;
 };
 
 int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cudaStream_t st, const Backward* bwd,
-                const E4m3Scales* f8 = nullptr) {
+                const Fp8Inputs* f8 = nullptr) {
     const grpo_shape& s = *in.shape;
     const bool bf16 = s.dtype == GRPO_BF16;
     const int row_bytes = f8 ? s.d : 2 * s.d;
@@ -467,7 +468,7 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_FWD, st, [&] {
-                return f8 ? launch_fwd_pair_e4m3(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, st)
+                return f8 ? launch_fwd_pair_fp8(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, f8->e5m2, st)
                           : launch_fwd_pair(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, bf16, st);
             }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
@@ -509,7 +510,7 @@ void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, gr
 size_t grpo_workspace_bytes(const grpo_shape* shape) {
     if (!shape) return 0;
     grpo_shape s = *shape;
-    if (s.dtype == GRPO_E4M3) s.dtype = GRPO_BF16;   // same layout; the 8-bit chunk copies use half
+    if (s.dtype == GRPO_E4M3 || s.dtype == GRPO_E5M2) s.dtype = GRPO_BF16;   // same layout; 8-bit chunks use half
     WsLayout L;
     if (!ws_layout(s, &L)) return 0;
     return L.total;
@@ -596,7 +597,7 @@ int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float
                       const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out, float* row_stats,
                       int32_t* status, grpo_stream_t stream) {
     if (!shape) return GRPO_ERR_SHAPE;
-    if (shape->dtype != GRPO_E4M3) return GRPO_ERR_DTYPE;
+    if (shape->dtype != GRPO_E4M3 && shape->dtype != GRPO_E5M2) return GRPO_ERR_DTYPE;
     if (shape->d % 128 != 0) return GRPO_ERR_SHAPE;
     if (!(scale_h_pol > 0.f) || !(scale_h_ref > 0.f) || !(scale_w > 0.f) || !std::isfinite(scale_h_pol) ||
         !std::isfinite(scale_h_ref) || !std::isfinite(scale_w))
@@ -611,7 +612,7 @@ int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != GRPO_OK) return rc;
-    const E4m3Scales f8{scale_h_pol, scale_h_ref, scale_w};
+    const Fp8Inputs f8{shape->dtype == GRPO_E5M2, scale_h_pol, scale_h_ref, scale_w};
     return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr, &f8);
 }
 

@@ -138,8 +138,8 @@ cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtenso
 // CTA-pair (M=256) variants: forward of a chunk, dH, dW
 cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
                             const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
-cudaError_t launch_fwd_pair_e4m3(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
-                                 const CUtensorMap& mW, int n_sm, cudaStream_t st);
+cudaError_t launch_fwd_pair_fp8(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
+                                const CUtensorMap& mW, int n_sm, bool e5m2, cudaStream_t st);
 cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm,
                            bool bf16, cudaStream_t st);
 cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,

@@ -159,9 +159,10 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool in_bf16
 
 // Instruction descriptor of kind::f8f6f4 with both operands E4M3 (format 0),
 // K-major, fp32 accumulation.
-__host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
+__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, bool e5m2) {
     return (1u << 4)                                   // D: f32
-           | (0u << 7) | (0u << 10)                    // A, B: E4M3
+           | ((e5m2 ? 1u : 0u) << 7)                   // A: E4M3 (0) or E5M2 (1)
+           | ((e5m2 ? 1u : 0u) << 10)                  // B: the same format
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

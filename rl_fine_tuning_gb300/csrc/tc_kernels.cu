@@ -672,9 +672,11 @@ struct FwdPairT {
     }
 };
 
-// The chunk forward on E4M3 inputs: the same tiles, byte for byte (a 128-byte
-// row holds 128 elements), a K-stage of 128 elements, four K=32 MMAs of kind
-// f8f6f4 per stage, and the per-tensor scales applied to the accumulator.
+// The chunk forward on 8-bit inputs (OCP E4M3, or E5M2 when kE5M2): the same
+// tiles, byte for byte (a 128-byte row holds 128 elements), a K-stage of 128
+// elements, four K=32 MMAs of kind f8f6f4 per stage, and the per-tensor scales
+// applied to the accumulator.
+template <bool kE5M2>
 struct FwdPairF8T : FwdPairT {
     static constexpr int kStageElems = 128;
     __device__ static bool setup(const Params& p, Sched& sc) {
@@ -689,7 +691,7 @@ struct FwdPairF8T : FwdPairT {
     }
     template <bool>
     __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
-        constexpr uint32_t idesc = make_idesc_e4m3(256, 256);
+        constexpr uint32_t idesc = make_idesc_f8(256, 256, kE5M2);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
             umma_pair_f8(acc, desc_kmajor(st + kk * 32), desc_kmajor(st + 16384 + kk * 32), idesc,
@@ -1099,7 +1101,8 @@ GRPO_TC_KERNEL(grpo_fwd_lse_kernel, FwdT)
     }
 
 GRPO_PAIR_KERNEL(grpo_fwd_pair_kernel, FwdPairT)
-GRPO_PAIR_KERNEL(grpo_fwd_pair_e4m3_kernel, FwdPairF8T)
+GRPO_PAIR_KERNEL(grpo_fwd_pair_e4m3_kernel, FwdPairF8T<false>)
+GRPO_PAIR_KERNEL(grpo_fwd_pair_e5m2_kernel, FwdPairF8T<true>)
 GRPO_PAIR_KERNEL(grpo_dh_pair_kernel, DhPairT)
 GRPO_PAIR_KERNEL(grpo_dw_pair_kernel, DwPairT)
 #undef GRPO_PAIR_KERNEL
@@ -1141,9 +1144,10 @@ cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CU
                 : launch_tc<FwdPairT, 2>(grpo_fwd_pair_kernel<false>, p, mHp, mHr, mW, n_sm, st);
 }
 
-cudaError_t launch_fwd_pair_e4m3(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
-                                 const CUtensorMap& mW, int n_sm, cudaStream_t st) {
-    return launch_tc<FwdPairF8T, 2>(grpo_fwd_pair_e4m3_kernel<true>, p, mHp, mHr, mW, n_sm, st);
+cudaError_t launch_fwd_pair_fp8(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
+                                const CUtensorMap& mW, int n_sm, bool e5m2, cudaStream_t st) {
+    return e5m2 ? launch_tc<FwdPairF8T<true>, 2>(grpo_fwd_pair_e5m2_kernel<true>, p, mHp, mHr, mW, n_sm, st)
+                : launch_tc<FwdPairF8T<false>, 2>(grpo_fwd_pair_e4m3_kernel<true>, p, mHp, mHr, mW, n_sm, st);
 }
 
 cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm, bool bf16,

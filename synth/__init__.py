@@ -55,6 +55,7 @@ def _L():
         lib.synth_to_bf16.argtypes = [p, i64, p]
         lib.synth_to_f16.argtypes = [p, i64, p]
         lib.synth_to_e4m3.argtypes = [p, i64, ctypes.c_float, p]
+        lib.synth_to_e5m2.argtypes = [p, i64, ctypes.c_float, p]
         _lib = lib
     return _lib
 
@@ -110,20 +111,31 @@ def to_f16_bits(x: np.ndarray) -> np.ndarray:
 
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
+FP8_MAX = {"e4m3": E4M3_MAX, "e5m2": E5M2_MAX}
+
+
+def fp8_scale(x: np.ndarray, fmt: str = "e4m3") -> float:
+    """Per-tensor scale that maps max|x| onto the largest finite value of the format."""
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    return float(np.float32(amax / FP8_MAX[fmt])) if amax > 0 else 1.0
 
 
 def e4m3_scale(x: np.ndarray) -> float:
-    """Per-tensor scale that maps max|x| onto the largest finite e4m3 value."""
-    amax = float(np.max(np.abs(x))) if x.size else 0.0
-    return float(np.float32(amax / E4M3_MAX)) if amax > 0 else 1.0
+    return fp8_scale(x, "e4m3")
+
+
+def to_fp8_bits(x: np.ndarray, scale: float, fmt: str = "e4m3") -> np.ndarray:
+    """fp32 values x -> OCP FP8 codes of x / scale (round to nearest even, saturating)."""
+    x = np.ascontiguousarray(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    fn = {"e4m3": _L().synth_to_e4m3, "e5m2": _L().synth_to_e5m2}[fmt]
+    fn(_ptr(x), x.size, scale, _ptr(out))
+    return out
 
 
 def to_e4m3_bits(x: np.ndarray, scale: float) -> np.ndarray:
-    """fp32 values x -> e4m3 codes of x / scale (round to nearest even, saturating)."""
-    x = np.ascontiguousarray(x, np.float32)
-    out = np.empty(x.shape, np.uint8)
-    _L().synth_to_e4m3(_ptr(x), x.size, scale, _ptr(out))
-    return out
+    return to_fp8_bits(x, scale, "e4m3")
 
 
 def bits_to_f32(b: np.ndarray, dtype: str) -> np.ndarray:
@@ -203,22 +215,28 @@ def rewards_for(cfg: Config, seed: int = 0) -> np.ndarray:
     return (b + normal_f32(seed, S_RNOISE, cfg.n_seq, 0.1)).astype(np.float32)
 
 
-def generate_e4m3(cfg: Config, seed: int = 0) -> Workload:
-    """The workload of `generate` quantised to e4m3 with one scale per tensor.
+def generate_fp8(cfg: Config, seed: int = 0, fmt: str = "e4m3") -> Workload:
+    """The workload of `generate` quantised to an OCP FP8 format ("e4m3" or
+    "e5m2") with one scale per tensor.
 
-    h_pol / h_ref / W hold e4m3 codes (uint8); extra["scales"] = (s_pol, s_ref, s_w)
-    with value = decode(code) * scale.  The reference rows are formed from the
-    unrounded policy rows, as in `generate`."""
+    h_pol / h_ref / W hold the codes (uint8); extra["scales"] = (s_pol, s_ref, s_w)
+    with value = decode(code) * scale, extra["fp8"] = fmt.  The reference rows
+    are formed from the unrounded policy rows, as in `generate`."""
     N, d, V = cfg.N, cfg.d, cfg.V
     h32 = normal_f32(seed, S_HPOL, N * d, 1.0)
     r32 = normal_f32(seed, S_REFNOISE, N * d, cfg.sigma_ref, base=h32)
     w32 = normal_f32(seed, S_W, V * d, cfg.w_sigma)
-    s_pol, s_ref, s_w = e4m3_scale(h32), e4m3_scale(r32), e4m3_scale(w32)
-    wl = Workload(cfg, to_e4m3_bits(h32, s_pol).reshape(N, d), to_e4m3_bits(r32, s_ref).reshape(N, d),
-                  to_e4m3_bits(w32, s_w).reshape(V, d), uniform_int(seed, S_TOK, N, 0, V - 1),
+    s_pol, s_ref, s_w = fp8_scale(h32, fmt), fp8_scale(r32, fmt), fp8_scale(w32, fmt)
+    wl = Workload(cfg, to_fp8_bits(h32, s_pol, fmt).reshape(N, d), to_fp8_bits(r32, s_ref, fmt).reshape(N, d),
+                  to_fp8_bits(w32, s_w, fmt).reshape(V, d), uniform_int(seed, S_TOK, N, 0, V - 1),
                   lengths_for(cfg, seed), rewards_for(cfg, seed))
     wl.extra["scales"] = (s_pol, s_ref, s_w)
+    wl.extra["fp8"] = fmt
     return wl
+
+
+def generate_e4m3(cfg: Config, seed: int = 0) -> Workload:
+    return generate_fp8(cfg, seed, "e4m3")
 
 
 def generate(cfg: Config, seed: int = 0, with_w: bool = True) -> Workload:

@@ -177,3 +177,43 @@ void synth_to_e4m3(const float* in, int64_t n, float scale, uint8_t* out) {
 #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e4m3(in[i] * inv);
 }
+
+/* fp32 -> OCP FP8 E5M2 bit pattern: 5 exponent bits (bias 15), 2 mantissa
+ * bits; round to nearest even, saturating to +-57344 (the format's infinities
+ * 0x7C / 0xFC and NaNs are never produced from finite inputs). */
+static uint8_t f32_to_e5m2(float xf) {
+    double x = (double)xf;
+    uint8_t sign = 0;
+    if (x < 0) { sign = 0x80; x = -x; }
+    if (x >= 57344.0) return (uint8_t)(sign | 0x7B);
+    if (x < ldexp(1.0, -17)) return sign;                 /* below half the smallest subnormal */
+    int e;
+    double m = frexp(x, &e);
+    int exp_unbiased = e - 1;
+    uint32_t code;
+    if (exp_unbiased < -14) {                             /* subnormal: units of 2^-16 */
+        double q = x / ldexp(1.0, -16);
+        double fl = floor(q);
+        double r = q - fl;
+        uint32_t n = (uint32_t)fl;
+        if (r > 0.5 || (r == 0.5 && (n & 1u))) n += 1;
+        code = n;                                         /* n == 4 is the smallest normal's code */
+    } else {
+        double q = (m * 2.0 - 1.0) * 4.0;
+        double fl = floor(q);
+        double r = q - fl;
+        uint32_t mant = (uint32_t)fl;
+        if (r > 0.5 || (r == 0.5 && (mant & 1u))) mant += 1;
+        uint32_t be = (uint32_t)(exp_unbiased + 15);
+        if (mant == 4) { mant = 0; be += 1; }
+        code = (be << 2) | mant;
+        if (code > 0x7B) code = 0x7B;
+    }
+    return (uint8_t)(sign | code);
+}
+
+void synth_to_e5m2(const float* in, int64_t n, float scale, uint8_t* out) {
+    const float inv = 1.0f / scale;
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = f32_to_e5m2(in[i] * inv);
+}

@@ -70,6 +70,8 @@ def test_shape_defaults_and_workspace_bytes(lib):
     assert n < 2 * 2 * N * V // 25          # > 25x below the two logit tensors
     s2 = rg.make_shape(1, 8, 20000, 4096, 128256, chunk_rows=4096)
     assert rg.grpo_workspace_bytes(s2) < n
+    for fp8 in (rg.E4M3, rg.E5M2):          # the 8-bit forward uses the 16-bit layout
+        assert rg.grpo_workspace_bytes(rg.make_shape(1, 8, 20000, 4096, 128256, fp8)) == n
     for bad in (dict(d=100), dict(d=0), dict(V=0), dict(G=0), dict(L=0)):
         b = rg.make_shape(1, 8, 20000, 4096, 128256)
         for k, v in bad.items():
@@ -93,6 +95,9 @@ def test_validation_codes_without_a_device(lib):
     assert f(*args[:6], ctypes.byref(bad), *args[7:]) == 2               # d not a multiple of 64
     bad.dtype = 7
     assert f(*args[:6], ctypes.byref(bad), *args[7:]) == 5               # unknown dtype
+    for fp8 in (rg.E4M3, rg.E5M2):                                       # 8-bit codes: grpo_loss_fwd_fp8 only
+        b8 = rg.make_shape(1, 4, 64, 128, 1024, fp8)
+        assert f(*args[:6], ctypes.byref(b8), *args[7:]) == 5
     for field, val in (("loss_mode", 2), ("objective", 4), ("objective", -1)):
         b2 = rg.make_shape(1, 4, 64, 128, 1024)
         setattr(b2, field, val)

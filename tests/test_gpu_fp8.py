@@ -1,6 +1,7 @@
-"""The E4M3 forward (grpo_loss_fwd_fp8) against the fp64 oracle on the same
-8-bit inputs: the oracle reads every code times its tensor's scale exactly in
-fp64, so this is the same parity bar as the 16-bit forward."""
+"""The 8-bit forward (grpo_loss_fwd_fp8, E4M3 and E5M2 inputs) against the
+fp64 oracle on the same 8-bit inputs: the oracle reads every code times its
+tensor's scale exactly in fp64, so this is the same parity bar as the 16-bit
+forward."""
 import numpy as np
 import pytest
 
@@ -20,7 +21,8 @@ from test_gpu_parity import assert_fwd_parity  # noqa: E402
 def run_fp8(wl8, mask=None, eval_rows=None):
     cfg = wl8.cfg
     s_pol, s_ref, s_w = wl8.extra["scales"]
-    shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.E4M3, beta=cfg.beta, eps=cfg.eps)
+    dtype = rg.E5M2 if wl8.extra.get("fp8") == "e5m2" else rg.E4M3
+    shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, dtype, beta=cfg.beta, eps=cfg.eps)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     h_pol, h_ref, W = dev(wl8.h_pol), dev(wl8.h_ref), dev(wl8.W)
     tokens, lengths, rewards = dev(wl8.tokens), dev(wl8.lengths), dev(wl8.rewards)
@@ -44,11 +46,12 @@ def run_fp8(wl8, mask=None, eval_rows=None):
     return res, exp
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("over", [dict(), dict(G=4, L=500, d=384, V=3000, len_lo=1, len_hi=500),
                                   dict(G=2, L=300, d=256, V=777, sigma_ref=0.4)])
-def test_fp8_forward_parity(over):
+def test_fp8_forward_parity(over, fmt):
     cfg = synth.make_config("tiny", **over)
-    res, exp = run_fp8(synth.generate_e4m3(cfg, seed=41))
+    res, exp = run_fp8(synth.generate_fp8(cfg, seed=41, fmt=fmt))
     assert np.array_equal(res["adv"].view(np.uint32), exp["adv"].view(np.uint32))
     assert_fwd_parity(res, exp)
 
@@ -71,9 +74,10 @@ def test_fp8_rejects_bad_arguments():
     del wl8
 
 
-def test_fp8_forward_full_size_sampled_rows():
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_forward_full_size_sampled_rows(fmt):
     cfg = synth.CONFIGS["llama-3.1-8b-head"]
-    wl8 = synth.generate_e4m3(cfg, seed=0)
+    wl8 = synth.generate_fp8(cfg, seed=0, fmt=fmt)
     mask = oracle.build_mask(wl8.lengths, cfg.L)
     rows = oracle.valid_rows(mask)
     rng = np.random.default_rng(5)

@@ -120,6 +120,47 @@ def test_generator_e4m3_rounding_brute_force():
     assert np.max(np.abs(oracle.e4m3_values(synth.to_e4m3_bits(x, s), s))) <= 448.0 * s * (1 + 1e-7)
 
 
+def test_e5m2_decoding_special_values():
+    """OCP FP8 E5M2: bias 15, 2 mantissa bits, IEEE-style infinities and NaNs."""
+    lib = oracle._L()
+    dec = np.array([lib.oracle_e5m2_to_f64(i) for i in range(256)])
+    assert dec[0x3C] == 1.0 and dec[0x7B] == 57344.0 and dec[0x04] == 2.0 ** -14 and dec[0x01] == 2.0 ** -16
+    assert dec[0x03] == 3 * 2.0 ** -16 and dec[0x40] == 2.0 and dec[0x3E] == 1.5 and dec[0x3F] == 1.75
+    assert dec[0x7C] == np.inf and dec[0xFC] == -np.inf
+    assert all(np.isnan(dec[c]) for c in (0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF))
+    assert dec[0x00] == 0.0 and np.signbit(dec[0x80])
+    assert np.array_equal(dec[0x80:0xFD], -dec[0x00:0x7D])
+    assert np.all(np.diff(dec[0x00:0x7D]) > 0)
+    # an E5M2 code is the high byte of an IEEE binary16 value: numpy's half decoder agrees on every code
+    half = (np.arange(256, dtype=np.uint16) << 8).view(np.float16).astype(np.float64)
+    finite = ~np.isnan(half)
+    assert np.array_equal(dec[finite], half[finite]) and np.array_equal(np.isnan(dec), ~finite)
+
+
+def test_generator_e5m2_rounding_brute_force():
+    """Each code is the nearest e5m2 value to x/scale (ties to an even mantissa), saturating at 57344."""
+    lib = oracle._L()
+    dec = np.array([lib.oracle_e5m2_to_f64(i) for i in range(256)])
+    pos = np.arange(0x7C)                                       # finite non-negative codes
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.normal(0, 3000, 4000), rng.uniform(-70000, 70000, 2000), rng.normal(0, 1e-4, 2000),
+                        dec[pos] + 0.5 * np.diff(np.append(dec[pos], 61440.0))])     # exact midpoints
+    x = x.astype(np.float32)
+    codes = synth.to_fp8_bits(x, 1.0, "e5m2")
+    for xi, c in zip(x.astype(np.float64), codes):
+        a = abs(xi)
+        err = np.abs(dec[pos] - min(a, 57344.0))
+        best = pos[err == err.min()]
+        if best.size > 1:
+            best = best[(best & 1) == 0]
+        assert (c & 0x7F) == best[0], (xi, hex(c), hex(best[0]))
+        if xi > 0:
+            assert c >> 7 == 0
+    s = synth.fp8_scale(x, "e5m2")
+    vals = oracle.fp8_values(synth.to_fp8_bits(x, s, "e5m2"), s, "e5m2")
+    assert np.all(np.isfinite(vals)) and np.max(np.abs(vals)) <= 57344.0 * s * (1 + 1e-7)
+
+
 def test_generator_is_counter_based():
     a = synth.normal_f32(0, 1, 1000)
     b = synth.normal_f32(0, 1, 500, offset=500)
