@@ -149,6 +149,26 @@ def test_fwd_bwd_scattered_mask():
     assert_grad_parity(res, exp)
 
 
+@pytest.mark.parametrize("over", [
+    dict(V=1),                                               # one vocabulary entry: softmax is 1, dS is 0
+    dict(d=64, V=200),                                       # smallest d, one partial vocabulary tile
+    dict(G=1, sigma_ref=0.3),                                # one completion: A = 0, only the KL term acts
+    dict(G=2, L=100, d=64, V=257 * 256, len_lo=40, len_hi=100),   # 257 vocabulary tiles: no even split exists
+])
+def test_degenerate_shapes(over):
+    cfg = synth.make_config("tiny", **over)
+    _, _, res, exp = _run(cfg, seed=11)
+    assert_fwd_parity(res, exp)
+    assert_grad_parity(res, exp)
+    if cfg.V == 1:
+        # lse = z, q = p = 0, and every dlogit is s*g*(1 - 1) = 0: the gradients are exactly zero
+        rows = exp["eval_rows"]
+        assert np.all(res["row_stats"][rows, 2:5] == 0)
+        assert np.all(res["dH"] == 0) and np.all(res["dW"] == 0)
+    if cfg.G == 1:
+        assert np.all(res["adv"] == 0)
+
+
 def test_kl_stress():
     cfg = synth.make_config("tiny", sigma_ref=0.5)
     _, _, res, exp = _run(cfg, seed=7)
