@@ -93,7 +93,7 @@ struct ChunkParams {
 };
 
 struct MergeParams {
-    const float4* part;     // by row (chunk < 0) or by chunk slot
+    const float4* part;     // [N x S] by row (chunk < 0), or [R x S] by chunk slot
     const float2* zt;
     const uint8_t* mask;
     const int* tokens;

@@ -219,29 +219,51 @@ cudaError_t launch_index(const uint8_t* mask, int64_t N, int R_max, int* counts,
 }
 
 // ------------------------------------------------------------ merge + objective
+// The split partials of one row, part[0 .. S), merged by one warp: lane k
+// takes splits k, k+32, ...; the maxima and then the rescaled sums are
+// combined across the warp in a fixed butterfly order.  Lane 0's results are
+// the ones used (every lane combines in its own order).
+__device__ __forceinline__ void merge_lse_warp(const float4* __restrict__ part, int S, int lane, float* lse_pol,
+                                               float* lse_ref) {
+    float mp = -INFINITY, mr = -INFINITY;
+    for (int k = lane; k < S; k += 32) {
+        const float4 ps = part[k];
+        mp = fmaxf(mp, ps.x);
+        mr = fmaxf(mr, ps.z);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+        mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+    }
+    float sp = 0.f, sr = 0.f;
+    for (int k = lane; k < S; k += 32) {
+        const float4 ps = part[k];
+        sp += ps.y * expf(ps.x - mp);
+        sr += ps.w * expf(ps.z - mr);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+        sr += __shfl_xor_sync(0xffffffffu, sr, o);
+    }
+    *lse_pol = mp + logf(sp);
+    *lse_ref = mr + logf(sr);
+}
+
 // Per row: merge the per-split (max, sum-exp) partials of the policy and the
 // reference logits into their logsumexp, form q, p, the reverse-KL term
 // exp(p-q) - (p-q) - 1 = expm1(x) - x, the per-token objective and its
 // derivative w.r.t. q ("Long-context GRPO", section 4).  The masked sum of the
-// objective is reduced in fp64 along a fixed tree.
-__device__ __forceinline__ float merge_lse(const float4* __restrict__ part, int S, bool ref) {
-    float m = -INFINITY;
-    for (int s = 0; s < S; ++s) m = fmaxf(m, ref ? part[s].z : part[s].x);
-    float acc = 0.f;
-    for (int s = 0; s < S; ++s) {
-        const float ms = ref ? part[s].z : part[s].x;
-        const float ss = ref ? part[s].w : part[s].y;
-        acc += ss * expf(ms - m);
-    }
-    return m + logf(acc);
-}
-
-// One thread per row: all rows t in [0, N) (chunk < 0), or the valid rows of
+// objective is reduced in fp64 along a fixed tree afterwards.
+// One warp per row: all rows t in [0, N) (chunk < 0), or the valid rows of
 // one backward chunk.  Writes lse_pol, g = d ell / d q and ell per row.
 __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
+    const int64_t row = (blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     int64_t t, pidx;
     if (p.chunk < 0) {
-        t = blockIdx.x * static_cast<int64_t>(kMergeThreads) + threadIdx.x;
+        t = row;
         if (t >= p.N) return;
         pidx = t;
     } else {
@@ -249,20 +271,18 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
         const int rc = p.counts[C_CHUNK_ROWS];
         const int c0 = p.chunk * rc;
         const int n_c = min(rc, p.counts[C_NVALID] - c0);
-        const int slot = blockIdx.x * kMergeThreads + threadIdx.x;
-        if (slot >= n_c) return;
-        t = p.rows[c0 + slot];
-        pidx = slot;
+        if (row >= n_c) return;
+        t = p.rows[c0 + row];
+        pidx = row;
     }
+    // t is uniform across the warp from here on
     float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, pen = 0.f, g = 0.f, ell = 0.f;
     if (p.mask[t]) {
         const int tok = p.tokens[t];
         if (tok < 0 || tok >= p.V) {
-            atomicCAS(p.status, 0, GRPO_ERR_SHAPE);
+            if (lane == 0) atomicCAS(p.status, 0, GRPO_ERR_SHAPE);
         } else {
-            const float4* pr = p.part + pidx * p.S;
-            lse_p = merge_lse(pr, p.S, false);
-            lse_r = merge_lse(pr, p.S, true);
+            merge_lse_warp(p.part + pidx * p.S, p.S, lane, &lse_p, &lse_r);
             const float2 z = p.zt[t];
             q = z.x - lse_p;
             p_ = z.y - lse_r;
@@ -309,6 +329,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
             }
         }
     }
+    if (lane != 0) return;
     p.lse[t] = lse_p;
     p.gco[t] = g;
     p.ell[t] = ell;
@@ -323,8 +344,9 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
 }
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
-    const int64_t n = p.chunk < 0 ? p.N : static_cast<int64_t>(p.R);
-    int64_t blocks = (n + kMergeThreads - 1) / kMergeThreads;
+    const int64_t n = p.chunk < 0 ? p.N : static_cast<int64_t>(p.R);   // rows, one warp each
+    constexpr int kRowsPerBlock = kMergeThreads / 32;
+    int64_t blocks = (n + kRowsPerBlock - 1) / kRowsPerBlock;
     if (blocks < 1) blocks = 1;
     k_merge<<<static_cast<unsigned>(blocks), kMergeThreads, 0, st>>>(p);
     return cudaGetLastError();
