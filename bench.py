@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--chunk-rows", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of one oracle sample")
     ap.add_argument("--forward", action="store_true",
                     help="time the forward-only entry points (bf16 and e4m3 inputs) instead of fwd+bwd")
@@ -353,6 +354,33 @@ def run_ours(args, ranks):
     ms_step = ms_max / args.steps
     value = ranks.world * n_valid * args.steps / (ms_max / 1e3)
 
+    # ---------------- the same step captured once into a CUDA graph and replayed
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(dev)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(dev)
+        g.replay()
+        torch.cuda.synchronize()
+        ranks.barrier()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        ms_g = ranks.max(g0.elapsed_time(g1))
+        graph = {"value": ranks.world * n_valid * args.steps / (ms_g / 1e3), "unit": "tokens/s",
+                 "ms_per_step": ms_g / args.steps, "what": "one step captured into a CUDA graph, replayed"}
+        del g
+
     # ---------------- end to end: host inputs copied in, loss read back, every step
     e2e = None
     if not args.no_e2e:
@@ -433,6 +461,7 @@ def run_ours(args, ranks):
         "workspace_gb": ws_bytes / 1e9,
         "logits_not_materialised_gb": 2 * 2 * N * V / 1e9,
         "e2e": e2e,
+        "graph": graph,
         "gpu_launches": int(launches),
         "kernels": kernels,
         "roofline": roofline,
