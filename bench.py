@@ -168,9 +168,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kind, config_name):
+def ncu_traffic(kind, chunk_rows):
     """DRAM bytes per launch of `kind` from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
+    taken on the current kernel source with chunks of the same height; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -178,7 +178,7 @@ def ncu_traffic(kind, config_name):
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("kernel_source_hash") != kernel_source_hash():
+    if d.get("kernel_source_hash") != kernel_source_hash() or d.get("chunk_rows") != chunk_rows:
         return None
     ent = d.get("kernels", {}).get(kind)
     if not ent:
@@ -435,7 +435,7 @@ def run_ours(args, ranks):
     achieved = flops_kind[dom] * args.steps / (dom_ms / 1e3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                 "frac": achieved / sustained, "peak_kind": f"bf16 dense sustained, {pk_kind}",
-                "traffic": ncu_traffic(dom, cfg.name),
+                "traffic": ncu_traffic(dom, rg.grpo_chunk_rows(shape)),
                 "traffic_per": "full chunk launch (ncu DRAM read+write bytes)",
                 "flops_per_launch": flops_kind[dom] * args.steps / dom_n, "ms_per_launch": dom_ms / dom_n}
     useful = 8.0 * n_valid * V * d
@@ -450,7 +450,7 @@ def run_ours(args, ranks):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ranks.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generator; random-init head)",
-        "config": cfg_dict(cfg, {"n_valid": n_valid, "chunk_rows": args.chunk_rows or 76 * 128,
+        "config": cfg_dict(cfg, {"n_valid": n_valid, "chunk_rows": rg.grpo_chunk_rows(shape),
                                  "loss_scale": scale[0]}),
         "pct_bf16_peak": {"useful_tflops": useful / t_step / 1e12,
                           "of_burst": useful / t_step / 1e12 / burst,

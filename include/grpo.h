@@ -71,8 +71,11 @@ typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
  *   beta        : KL coefficient (0.04 in the pages' setting)
  *   eps         : added to the group std in grpo_group_advantages
  *   std_unbiased: 1 -> group std with divisor G-1, 0 -> divisor G
- *   chunk_rows  : masked rows processed per backward chunk (0 -> 9728, i.e.
- *                 76 tiles of 128 rows); rounded up to a multiple of 128.
+ *   chunk_rows  : masked rows processed per backward chunk, rounded up to a
+ *                 multiple of 128 and capped at N.  0 picks the default: 38
+ *                 tiles of 128 rows (4864) when its dH work divides evenly
+ *                 over the 76 SM pairs (d/256 a multiple of 4, e.g. d = 4096
+ *                 or 5120), else 76 tiles (9728).  grpo_chunk_rows tells.
  *   loss_mode   : GRPO_TOKEN_MEAN -- mean of ell_t over all masked rows;
  *                 GRPO_SEQUENCE_MEAN -- mean over completions (with at least
  *                 one masked row) of each completion's mean over its rows
@@ -108,6 +111,12 @@ void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, gr
  * shape: O(chunk_rows * (V + d) + N), independent of how many rows are
  * masked.  Returns 0 for an invalid shape. */
 size_t grpo_workspace_bytes(const grpo_shape* shape);
+
+/* Rows per backward chunk that grpo_loss_fwd / grpo_loss_fwd_bwd use for this
+ * shape (the chunk_rows field resolved as described above).  Returns 0 for
+ * an invalid shape.  The pages have no counterpart: it is this library's
+ * memory/throughput knob. */
+int grpo_chunk_rows(const grpo_shape* shape);
 
 /* Group-relative advantages ("Train your own R1 reasoning model with
  * Unsloth", section 3, steps 3-5: score each response, take the group mean,

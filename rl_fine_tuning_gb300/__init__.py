@@ -141,6 +141,10 @@ def grpo_workspace_bytes(shape: GrpoShape) -> int:
     return int(load().grpo_workspace_bytes(ctypes.byref(shape)))
 
 
+def grpo_chunk_rows(shape: GrpoShape) -> int:
+    return int(load().grpo_chunk_rows(ctypes.byref(shape)))
+
+
 def grpo_group_advantages(rewards, n_groups, G, eps, std_unbiased, adv_out, stream=None):
     _check(load().grpo_group_advantages(_ptr(rewards), n_groups, G, eps, int(bool(std_unbiased)), _ptr(adv_out),
                                         _stream(stream)), "grpo_group_advantages")

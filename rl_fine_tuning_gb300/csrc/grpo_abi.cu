@@ -146,8 +146,15 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
     return r == CUDA_SUCCESS;
 }
 
+int default_chunk_rows(const grpo_shape& s) {
+    const int n_dt = (s.d + kBN - 1) / kBN;
+    const int pairs_small = (kChunkTilesSmall + 1) / 2;
+    const int tiles = (pairs_small * n_dt) % kChunkPairs == 0 ? kChunkTilesSmall : kChunkTilesLarge;
+    return tiles * kBM;
+}
+
 int chunk_rows_of(const grpo_shape& s) {
-    int r = s.chunk_rows > 0 ? s.chunk_rows : kDefaultChunkRows;
+    int r = s.chunk_rows > 0 ? s.chunk_rows : default_chunk_rows(s);
     r = (r + kBM - 1) / kBM * kBM;
     const int64_t N = static_cast<int64_t>(s.n_groups) * s.G * s.L;
     const int64_t nmax = (N + kBM - 1) / kBM * kBM;
@@ -505,6 +512,11 @@ void grpo_shape_init(grpo_shape* s, int n_groups, int G, int L, int d, int V, gr
     s->chunk_rows = 0;
     s->loss_mode = GRPO_TOKEN_MEAN;
     s->objective = GRPO_OBJ_GRPO;
+}
+
+int grpo_chunk_rows(const grpo_shape* shape) {
+    if (!shape || !shape_ok(*shape)) return 0;
+    return chunk_rows_of(*shape);
 }
 
 size_t grpo_workspace_bytes(const grpo_shape* shape) {

@@ -15,10 +15,15 @@ constexpr int kBN = 256;              // accumulator columns per MMA tile
 constexpr int kTileSplits = 8;        // vocabulary splits of a forward row tile (forward-only path)
 constexpr int kChunkSplits = 64;      // vocabulary splits of a chunk row tile (forward+backward path), target
 constexpr int kChunkSplitsMax = 256;  // ... and the most it may take to divide the vocabulary tiles evenly
-// Default rows per backward chunk: 76 tiles of 128.  On 152 SMs (76 CTA pairs)
-// the chunk's forward units (76 tiles x 64 splits) and its dH units (38 tile
-// pairs x d/256 tiles, for d = 1536, 4096 or 5120) divide evenly over the pairs.
-constexpr int kDefaultChunkRows = 76 * 128;
+// Default rows per backward chunk, in 128-row tiles: the smaller of 38 and 76
+// whose dH units ((tiles / 2) tile pairs x ceil(d / 256) d tiles) divide
+// evenly over the 76 SM pairs of a GB300 (38 for d = 4096 or 5120, 76 for
+// d = 1536).  Smaller chunks than that leave dH a part-empty last wave; larger
+// ones hold more dlogits memory and ran slower (a larger, busier working set
+// under the power cap).
+constexpr int kChunkPairs = 76;
+constexpr int kChunkTilesSmall = 38;
+constexpr int kChunkTilesLarge = 76;
 constexpr int kMergeThreads = 256;
 constexpr int kIndexThreads = 1024;
 constexpr int kTransformThreads = 256;

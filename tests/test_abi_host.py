@@ -63,13 +63,19 @@ def test_shape_defaults_and_workspace_bytes(lib):
     assert (s.beta, s.std_unbiased, s.chunk_rows) == (pytest.approx(0.04), 1, 0)
     assert s.eps == pytest.approx(1e-4)
     n = rg.grpo_workspace_bytes(s)
-    N, R, V, d = 160000, 76 * 128, 128256, 4096
+    N, R, V, d = 160000, 38 * 128, 128256, 4096
+    assert rg.grpo_chunk_rows(s) == R      # d/256 = 16: 19 tile pairs x 16 d tiles = 4 x 76 dH units
     # O(R*V + R*d + N) -- never O(N*V): dlogits chunk, two compact hidden-state chunks,
     # per-32-column maxima, per-split partials, per-row arrays
     assert R * V * 2 <= n < R * V * 2 + 2 * R * d * 2 + R * ((V + 31) // 32) * 4 + R * 256 * 16 + 300 * N + (1 << 20)
-    assert n < 2 * 2 * N * V // 25          # > 25x below the two logit tensors
+    assert n < 2 * 2 * N * V // 50          # > 50x below the two logit tensors
     s2 = rg.make_shape(1, 8, 20000, 4096, 128256, chunk_rows=4096)
-    assert rg.grpo_workspace_bytes(s2) < n
+    assert rg.grpo_workspace_bytes(s2) < n and rg.grpo_chunk_rows(s2) == 4096
+    assert rg.grpo_chunk_rows(rg.make_shape(1, 8, 4096, 1536, 151936)) == 76 * 128   # 6 d tiles: 76 tiles balance
+    assert rg.grpo_chunk_rows(rg.make_shape(1, 8, 8192, 5120, 100352)) == 38 * 128
+    assert rg.grpo_chunk_rows(rg.make_shape(1, 8, 20000, 4096, 128256, chunk_rows=100)) == 128
+    assert rg.grpo_chunk_rows(rg.make_shape(1, 4, 64, 128, 1024)) == 256            # capped at N
+    assert rg.grpo_chunk_rows(rg.make_shape(1, 8, 20000, 100, 128256)) == 0         # invalid shape
     for fp8 in (rg.E4M3, rg.E5M2):          # the 8-bit forward uses the 16-bit layout
         assert rg.grpo_workspace_bytes(rg.make_shape(1, 8, 20000, 4096, 128256, fp8)) == n
     for bad in (dict(d=100), dict(d=0), dict(V=0), dict(G=0), dict(L=0)):
