@@ -382,32 +382,73 @@ def run_ours(args, ranks):
         del g
 
     # ---------------- end to end: host inputs copied in, loss read back, every step
+    # Two ways, both through the public API with every step's inputs copied from
+    # pinned host memory inside the timed region: serially before each step, and
+    # overlapped the way a training loop prefetches its next batch (step i+1's
+    # inputs copied on a second stream into a second device buffer set while
+    # step i computes).  The overlapped figure is the headline.
     e2e = None
     if not args.no_e2e:
         loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
         h2d = sum(host[k].numel() * host[k].element_size() for k in host)
         d2h = 4
+        dev2 = {k: torch.empty_like(v) for k, v in dev.items()}
 
-        def e2e_step():
+        def copy_in(d_in):
             for k in host:
-                dev_raw = dev[k].view(host[k].dtype) if k in ("h_pol", "h_ref") else dev[k]
+                dev_raw = d_in[k].view(host[k].dtype) if k in ("h_pol", "h_ref") else d_in[k]
                 dev_raw.copy_(host[k], non_blocking=True)
-            step(dev)
-            loss_host.copy_(loss, non_blocking=True)
 
-        e2e_step()
-        torch.cuda.synchronize()
-        ranks.barrier()
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        a1.record(stream)
-        torch.cuda.synchronize()
-        ms_e2e = ranks.max(a0.elapsed_time(a1))
-        e2e = {"value": ranks.world * n_valid * args.steps / (ms_e2e / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e / args.steps,
+        def run_serial(n):
+            for _ in range(n):
+                copy_in(dev)
+                step(dev)
+                loss_host.copy_(loss, non_blocking=True)
+
+        copy_stream = torch.cuda.Stream()
+        bufs = (dev, dev2)
+        copied = [torch.cuda.Event() for _ in bufs]
+        consumed = [torch.cuda.Event() for _ in bufs]
+
+        def run_overlapped(n):
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                copy_in(bufs[0])
+                copied[0].record(copy_stream)
+            for i in range(n):
+                b = i % 2
+                if i + 1 < n:
+                    nb = (i + 1) % 2
+                    with torch.cuda.stream(copy_stream):
+                        if i >= 1:
+                            copy_stream.wait_event(consumed[nb])   # step i-1 has finished with that buffer
+                        copy_in(bufs[nb])
+                        copied[nb].record(copy_stream)
+                stream.wait_event(copied[b])
+                step(bufs[b])
+                consumed[b].record(stream)
+                loss_host.copy_(loss, non_blocking=True)
+
+        def timed(fn):
+            fn(1)
+            torch.cuda.synchronize()
+            ranks.barrier()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            fn(args.steps)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            return ranks.max(a0.elapsed_time(a1))
+
+        ms_ser = timed(run_serial)
+        ms_ovl = timed(run_overlapped)
+        del dev2
+        e2e = {"value": ranks.world * n_valid * args.steps / (ms_ovl / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h, "ms_per_step": ms_ovl / args.steps,
+               "copies": "step i+1's inputs copied on a second stream during step i (two device input sets)",
+               "serial": {"value": ranks.world * n_valid * args.steps / (ms_ser / 1e3),
+                          "ms_per_step": ms_ser / args.steps, "copies": "before each step, same stream"},
                "resident": "lm_head weight W"}
 
     # ---------------- roofline of the dominant kernel

@@ -503,7 +503,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
 // group the a-indices are fastest.  With G = 1 the b-index is fastest.  The
 // group sizes were chosen by timing on GB300 (16 row tiles per group for the
 // chunk forward: each W tile is then shared in L2 by 16 tiles).
-constexpr int kFwdGroup = 16;   // chunk forward: a = 128-row tile, b = vocabulary split
+constexpr int kFwdGroup = 19;   // chunk forward: a = 128-row tile, b = vocabulary split (19 divides 38 and 76)
 constexpr int kDhGroup = 1;     // dH: a = pair of 128-row tiles, b = 256-wide d tile
 constexpr int kDwGroup = 1;     // dW: a = pair of 128-row vocabulary tiles, b = 256-wide d tile
 
