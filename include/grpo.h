@@ -54,7 +54,9 @@ enum {
     GRPO_ERR_LAUNCH = 4,     /* a CUDA launch or driver call failed */
     GRPO_ERR_DTYPE = 5,      /* dtype not supported */
     GRPO_ERR_TIMEOUT = 6,    /* a device-side wait ran out of time (kernel gave up, no hang) */
-    GRPO_ERR_DEVICE = 7      /* device is not sm_103 / lacks the needed shared memory */
+    GRPO_ERR_DEVICE = 7,     /* device is not sm_103 / lacks the needed shared memory */
+    GRPO_ERR_BOUNDS = 8      /* a device-side index check failed; only the checked build
+                                (libgrpo_checked.so, see grpo_device_checks) makes them */
 };
 
 typedef enum { GRPO_BF16 = 0, GRPO_FP16 = 1, GRPO_E4M3 = 2, GRPO_E5M2 = 3 } grpo_dtype;
@@ -248,6 +250,19 @@ enum {
 int grpo_profile_enable(int on);
 int grpo_profile_collect(double* ms, long long* launches, int n_kinds);
 unsigned long long grpo_kernel_launches(void);
+
+/* Device-side index checks.  The library is also built as
+ * libgrpo_checked.so, whose kernels check every global index they take from
+ * device data (the valid-row list) and the offset arithmetic of the chunk
+ * buffers: a failing check skips the access and sets *status to
+ * GRPO_ERR_BOUNDS.  It stands in for a memory checker; the pages have no
+ * counterpart.  grpo_device_checks() returns 1 in that build, 0 in the normal
+ * one.  grpo_selftest_bounds_check makes one such check fail on purpose (a
+ * guarded store one past a 16-element shared array, refused by the check):
+ * *status (device int32) then reads GRPO_ERR_BOUNDS.  In the normal build it
+ * launches nothing and returns GRPO_ERR_DEVICE. */
+int grpo_device_checks(void);
+int grpo_selftest_bounds_check(int32_t* status, grpo_stream_t stream);
 
 /* Self-test of the bounded device waits: one CTA waits, with the wait the
  * kernels use, on an mbarrier that nothing completes.  It gives up after about

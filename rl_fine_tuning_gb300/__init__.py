@@ -223,6 +223,19 @@ def grpo_loss_fwd_fp8(h_pol, h_ref, W, scale_h_pol, scale_h_ref, scale_w, tokens
               _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_fp8")
 
 
+def grpo_device_checks() -> bool:
+    """True when the loaded library is the build with device-side index checks."""
+    return bool(load().grpo_device_checks())
+
+
+def grpo_selftest_bounds_check(status, stream=None):
+    fn = load().grpo_selftest_bounds_check
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    _check(fn(_ptr(status), _stream(stream)), "grpo_selftest_bounds_check")
+
+
 def grpo_selftest_wait_timeout(status, waited_ns, stream=None):
     fn = load().grpo_selftest_wait_timeout
     if fn.argtypes is None:

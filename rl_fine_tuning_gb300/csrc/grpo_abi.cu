@@ -436,6 +436,7 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     fp.part = reinterpret_cast<float4*>(w + L.partc);
     fp.S = L.Sc;
     fp.nps = L.npsc;
+    fp.R = L.R;
     // the exponentials are kept only when a backward follows
     fp.E = bwd ? static_cast<uint16_t*>(ds) : nullptr;
     fp.mx = bwd ? reinterpret_cast<float*>(w + L.mx) : nullptr;
@@ -457,6 +458,8 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     cp.d = s.d;
     cp.V_pad = L.V_pad;
     cp.nc32 = L.nc32;
+    cp.R = L.R;
+    cp.N = L.N;
     cp.dS = static_cast<uint16_t*>(ds);
     cp.dH = bwd ? static_cast<uint16_t*>(bwd->dH) : nullptr;
     cp.dW = bwd ? bwd->dW : nullptr;
@@ -628,6 +631,28 @@ int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float
     return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr, &f8);
 }
 
+int grpo_device_checks(void) {
+#ifdef GRPO_DEVICE_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+int grpo_selftest_bounds_check(int32_t* status, grpo_stream_t stream) {
+    if (!status || !aligned(status, 4)) return GRPO_ERR_POINTER;
+#ifdef GRPO_DEVICE_CHECKS
+    DeviceInfo dev;
+    const int rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    if (launch_bounds_selftest(status, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return GRPO_ERR_LAUNCH;
+    return GRPO_OK;
+#else
+    (void)stream;
+    return GRPO_ERR_DEVICE;   // built without device checks: nothing is launched
+#endif
+}
+
 int grpo_selftest_wait_timeout(int32_t* status, unsigned long long* waited_ns, grpo_stream_t stream) {
     if (!status || !waited_ns || !aligned(status, 4) || !aligned(waited_ns, 8)) return GRPO_ERR_POINTER;
     DeviceInfo dev;
@@ -648,6 +673,7 @@ const char* grpo_status_string(int status) {
         case GRPO_ERR_DTYPE: return "unsupported dtype";
         case GRPO_ERR_TIMEOUT: return "device wait timed out";
         case GRPO_ERR_DEVICE: return "device is not an sm_103 GPU with enough shared memory";
+        case GRPO_ERR_BOUNDS: return "device index check failed (checked build)";
         default: return "unknown status";
     }
 }

@@ -9,6 +9,22 @@
 
 namespace grpo {
 
+// Device-side index checks of the checked build (compiled with
+// GRPO_DEVICE_CHECKS): GRPO_DCHECK(cond, status) is cond, and a false cond
+// also records GRPO_ERR_BOUNDS in the caller's status word; the caller then
+// skips the access.  In the normal build it is the constant true and costs
+// nothing.  The checks cover every global index a kernel takes from device
+// data (the valid-row list) and the offset arithmetic of the chunk buffers.
+#ifdef GRPO_DEVICE_CHECKS
+__device__ inline bool dcheck(bool ok, int* status) {
+    if (!ok) atomicCAS(status, 0, GRPO_ERR_BOUNDS);
+    return ok;
+}
+#define GRPO_DCHECK(cond, status) ::grpo::dcheck((cond), (status))
+#else
+#define GRPO_DCHECK(cond, status) true
+#endif
+
 constexpr int kBM = 128;              // rows (or vocabulary rows for dW) per MMA tile
 constexpr int kBK = 64;               // K elements per pipeline stage: one 128-byte swizzle span
 constexpr int kBN = 256;              // accumulator columns per MMA tile
@@ -75,6 +91,7 @@ struct FwdParams {
     int64_t N;
     int chunk;
     int V, d, S, nps, n_ntiles, V_pad, nc32;
+    int R;                  // chunk mode: rows of the chunk buffers (index checks)
     int* status;
 };
 
@@ -89,6 +106,8 @@ struct ChunkParams {
     float scale;            // loss scale
     int chunk;
     int V, d, V_pad, nc32;
+    int R;                  // rows of the chunk buffers
+    int64_t N;              // rows of h_pol / dH (index checks)
     uint16_t* dS;           // [R x V_pad] scaled dlogits (without the 1/N_valid factor)
     uint16_t* dH;           // [N x d]
     float* dW;              // [V x d]
@@ -138,6 +157,9 @@ cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cudaStream_t st);
+#ifdef GRPO_DEVICE_CHECKS
+cudaError_t launch_bounds_selftest(int* status, cudaStream_t st);
+#endif
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
                        const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
 // CTA-pair (M=256) variants: forward of a chunk, dH, dW

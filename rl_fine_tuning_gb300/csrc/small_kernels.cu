@@ -172,8 +172,12 @@ __global__ void __launch_bounds__(kIndexThreads) k_index(const uint8_t* __restri
                 if (!((bits >> k) & 1u)) {
                     lzr = t;
                 } else {
-                    rows[vi++] = t;
-                    if (((t - lzr - 1) & (kBM - 1)) == 0) tiles[ti++] = make_int2(t, 0);
+                    if (GRPO_DCHECK(vi < N, status)) rows[vi] = t;
+                    ++vi;
+                    if (((t - lzr - 1) & (kBM - 1)) == 0) {
+                        if (GRPO_DCHECK(ti < N, status)) tiles[ti] = make_int2(t, 0);
+                        ++ti;
+                    }
                 }
             }
         }
@@ -271,9 +275,10 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
         const int rc = p.counts[C_CHUNK_ROWS];
         const int c0 = p.chunk * rc;
         const int n_c = min(rc, p.counts[C_NVALID] - c0);
-        if (row >= n_c) return;
+        if (row >= n_c || !GRPO_DCHECK(row < p.R, p.status)) return;
         t = p.rows[c0 + row];
         pidx = row;
+        if (!GRPO_DCHECK(t >= 0 && t < p.N, p.status)) return;   // uniform across the warp
     }
     // t is uniform across the warp from here on
     float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, pen = 0.f, g = 0.f, ell = 0.f;
@@ -449,7 +454,7 @@ cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, in
 // are zeroed.
 __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restrict__ rows, int chunk,
                               const uint4* __restrict__ h, uint4* __restrict__ hc, const uint4* __restrict__ hr,
-                              uint4* __restrict__ hcr, int vec_per_row, int R) {
+                              uint4* __restrict__ hcr, int vec_per_row, int R, int64_t N, int* status) {
     if (chunk >= counts[C_NCHUNKS]) return;
     const int rc = counts[C_CHUNK_ROWS];
     const int c0 = chunk * rc;
@@ -461,7 +466,7 @@ __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restr
         const int slot = static_cast<int>(i / vec_per_row);
         const int v = static_cast<int>(i - static_cast<int64_t>(slot) * vec_per_row);
         uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
-        if (slot < n_c) {
+        if (slot < n_c && GRPO_DCHECK(rows[c0 + slot] >= 0 && rows[c0 + slot] < N, status)) {
             const int64_t src = static_cast<int64_t>(rows[c0 + slot]) * vec_per_row + v;
             x = h[src];
             if (hr) y = hr[src];
@@ -471,6 +476,23 @@ __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restr
     }
 }
 
+#ifdef GRPO_DEVICE_CHECKS
+// One thread stores one past the end of a 16-element shared array through the
+// checked access pattern of the kernels: the check refuses the store and
+// records GRPO_ERR_BOUNDS.  Exists only in the checked build.
+__global__ void k_bounds_selftest(int* status) {
+    __shared__ int buf[16];
+    *status = 0;
+    const int i = 16 + static_cast<int>(threadIdx.x);
+    if (GRPO_DCHECK(i < 16, status)) buf[i] = 1;
+}
+
+cudaError_t launch_bounds_selftest(int* status, cudaStream_t st) {
+    k_bounds_selftest<<<1, 1, 0, st>>>(status);
+    return cudaGetLastError();
+}
+#endif
+
 cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
                                int row_bytes, cudaStream_t st) {
     const int vpr = row_bytes / 16;
@@ -479,7 +501,7 @@ cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc
     if (blocks > 152 * 16) blocks = 152 * 16;
     k_gather_rows<<<blocks, 256, 0, st>>>(p.counts, p.rows, p.chunk, static_cast<const uint4*>(h_pol),
                                           static_cast<uint4*>(hc), static_cast<const uint4*>(h_ref),
-                                          static_cast<uint4*>(hcr), vpr, R);
+                                          static_cast<uint4*>(hcr), vpr, R, p.N, p.status);
     return cudaGetLastError();
 }
 
@@ -507,6 +529,7 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform(const ChunkPara
             continue;
         }
         const int t = p.rows[c0 + slot];
+        if (!GRPO_DCHECK(t >= 0 && t < p.N, p.status)) continue;
         const int tok = p.tokens[t];
         const float lse = p.lse[t];
         const float coef = p.scale * p.gco[t];

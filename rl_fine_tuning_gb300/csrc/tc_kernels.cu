@@ -116,34 +116,21 @@ struct FwdT {
     using Params = FwdParams;
     struct Sched {
         int n_units, ks, n_tiles, C;
-        int c0, n_c;           // chunk mode: first valid-row index and rows of the chunk
-        bool chunked;
     };
     struct Coord {
         int t0, n0;
     };
     struct Epi {
         float m[2], s[2], zt[2];
-        int tok, t, split, slot;
+        int tok, t, split;
         bool valid, found;
     };
 
-    // unit = tile group * S + split; the tile of rank r is group * C + r.
-    // Tile mode: forward row tiles over h_pol/h_ref.  Chunk mode: 128-row tiles
-    // of the chunk's compact copies.
+    // unit = tile group * S + split; the tile of rank r is group * C + r.  Tiles
+    // are the forward row tiles over h_pol/h_ref (runs of masked-in rows).
     __device__ static bool setup(const Params& p, Sched& sc, int C) {
         sc.C = C;
-        sc.chunked = p.tiles == nullptr;
-        if (sc.chunked) {
-            if (p.chunk >= p.counts[C_NCHUNKS]) return false;
-            const int rc = p.counts[C_CHUNK_ROWS];
-            sc.c0 = p.chunk * rc;
-            sc.n_c = min(rc, p.counts[C_NVALID] - sc.c0);
-            sc.n_tiles = (sc.n_c + kBM - 1) / kBM;
-        } else {
-            sc.c0 = sc.n_c = 0;
-            sc.n_tiles = p.counts[C_NTILES];
-        }
+        sc.n_tiles = p.counts[C_NTILES];
         sc.n_units = ((sc.n_tiles + C - 1) / C) * p.S;
         sc.ks = p.d / kBK;
         return sc.n_units > 0;
@@ -161,10 +148,7 @@ struct FwdT {
     __device__ static Coord coord(const Params& p, const Sched& sc, int unit, int item, int rank) {
         Coord c;
         const int tile = tile_of(p, sc, unit, rank);
-        if (sc.chunked)
-            c.t0 = tile * kBM;
-        else
-            c.t0 = tile < sc.n_tiles ? p.tiles[tile].x : static_cast<int>(p.N);   // phantom: rows past the end
+        c.t0 = tile < sc.n_tiles ? p.tiles[tile].x : static_cast<int>(p.N);   // phantom: rows past the end
         c.n0 = ((unit % p.S) * p.nps + item) * kBN;
         return c;
     }
@@ -195,18 +179,10 @@ struct FwdT {
         const int tile = tile_of(p, sc, unit, rank);
         e.valid = false;
         e.t = 0;
-        e.slot = -1;
-        if (sc.chunked) {
-            const int slot = tile * kBM + row;
-            if (slot < sc.n_c) {
-                e.valid = true;
-                e.slot = slot;
-                e.t = p.rows[sc.c0 + slot];
-            }
-        } else if (tile < sc.n_tiles) {
+        if (tile < sc.n_tiles) {
             const int2 tl = p.tiles[tile];
             e.t = tl.x + row;
-            e.valid = row < tl.y;
+            e.valid = row < tl.y && GRPO_DCHECK(e.t >= 0 && e.t < p.N, p.status);
         }
         e.tok = e.valid ? p.tokens[e.t] : -1;
         e.split = unit % p.S;
@@ -216,13 +192,9 @@ struct FwdT {
         e.found = false;
     }
     template <bool kBf16>
-    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int item, int, uint32_t tacc,
+    __device__ static void epi_item(const Params& p, const Sched&, int unit, int item, int, uint32_t tacc,
                                     Epi& e) {
         const int n0 = ((unit % p.S) * p.nps + item) * kBN;
-        // chunk mode keeps the policy exponentials for the backward
-        const bool keep = sc.chunked && p.E != nullptr && e.valid;
-        uint16_t* erow = keep ? p.E + static_cast<int64_t>(e.slot) * p.V_pad : nullptr;
-        float* mrow = keep ? p.mx + static_cast<int64_t>(e.slot) * p.nc32 : nullptr;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
 #pragma unroll 1
@@ -257,22 +229,12 @@ struct FwdT {
                 }
                 e.s[w] = fmaf(e.s[w], fast_exp2(fmaf(e.m[w], kLog2e, -mb)), acc);
                 e.m[w] = m_new;
-                if (w == 0 && keep) {
-                    uint4* o4 = reinterpret_cast<uint4*>(erow + col0);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        o4[j] = make_uint4(pack2(v[8 * j], v[8 * j + 1], true), pack2(v[8 * j + 2], v[8 * j + 3], true),
-                                           pack2(v[8 * j + 4], v[8 * j + 5], true),
-                                           pack2(v[8 * j + 6], v[8 * j + 7], true));
-                    mrow[col0 >> 5] = m_new;
-                }
             }
         }
     }
-    __device__ static void epi_end(const Params& p, const Sched& sc, int, Epi& e) {
+    __device__ static void epi_end(const Params& p, const Sched&, int, Epi& e) {
         if (!e.valid) return;
-        const int64_t idx = sc.chunked ? static_cast<int64_t>(e.slot) : static_cast<int64_t>(e.t);
-        p.part[idx * p.S + e.split] = make_float4(e.m[0], e.s[0], e.m[1], e.s[1]);
+        p.part[static_cast<int64_t>(e.t) * p.S + e.split] = make_float4(e.m[0], e.s[0], e.m[1], e.s[1]);
         if (e.found) p.zt[e.t] = make_float2(e.zt[0], e.zt[1]);
     }
 };
@@ -584,8 +546,9 @@ struct FwdPairT {
         int mt, split;
         decode_tile_split(unit, sc.n_mt, p.S, &mt, &split);
         e.slot = mt * kBM + row;
-        e.valid = e.slot < sc.n_c;
+        e.valid = e.slot < sc.n_c && GRPO_DCHECK(e.slot < p.R, p.status);
         e.t = e.valid ? p.rows[sc.c0 + e.slot] : 0;
+        if (e.valid && !GRPO_DCHECK(e.t >= 0 && e.t < p.N, p.status)) e.valid = false;
         e.tok = e.valid ? p.tokens[e.t] : -1;
         e.split = split;
         e.m = -INFINITY;
@@ -642,7 +605,7 @@ struct FwdPairT {
             }
             e.s = fmaf(e.s, fast_exp2(fmaf(e.m, kLog2e, -mb)), acc);
             e.m = m_new;
-            if (keep) {
+            if (keep && GRPO_DCHECK(col0 + 32 <= p.V_pad, p.status)) {
                 // 64 bytes of one row as two whole 32-byte sectors
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -658,14 +621,14 @@ struct FwdPairT {
             }
         }
         // the row pitch of mx is a multiple of 8 groups and n0 of 256 columns: 32-byte aligned
-        if (keep)
+        if (keep && GRPO_DCHECK((n0 >> 5) + kBN / 32 <= p.nc32, p.status))
             st_global_v8(mrow + (n0 >> 5), __float_as_uint(mv[0]), __float_as_uint(mv[1]), __float_as_uint(mv[2]),
                          __float_as_uint(mv[3]), __float_as_uint(mv[4]), __float_as_uint(mv[5]),
                          __float_as_uint(mv[6]), __float_as_uint(mv[7]));
     }
     // the leader writes the policy half of the partials, the peer the reference half
     __device__ static void epi_end(const Params& p, const Sched&, int rank, Epi& e) {
-        if (!e.valid) return;
+        if (!e.valid || !GRPO_DCHECK(e.split >= 0 && e.split < p.S, p.status)) return;
         float* part = reinterpret_cast<float*>(p.part + static_cast<int64_t>(e.slot) * p.S + e.split);
         *reinterpret_cast<float2*>(part + 2 * rank) = make_float2(e.m, e.s);
         if (e.found) reinterpret_cast<float*>(p.zt + e.t)[rank] = e.zt;
@@ -763,9 +726,10 @@ struct DhPairT {
         const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
         const int slot = mtile(sc, unit, rank) * kBM + row;
         const int n0 = dtile(sc, unit) * kBN;
-        const bool valid = slot < sc.n_c;
+        bool valid = slot < sc.n_c;
         if (!__any_sync(0xffffffffu, valid)) return;
         const int t = valid ? p.rows[sc.c0 + slot] : 0;
+        if (valid && !GRPO_DCHECK(t >= 0 && t < p.N, p.status)) valid = false;
         uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
         bool bad = false;
 #pragma unroll 1

@@ -36,6 +36,18 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= exported
 
 
+def test_checked_build_exports_the_same_symbols_and_says_so(lib):
+    from rl_fine_tuning_gb300 import build
+    names = declared_functions()
+    checked = ctypes.CDLL(build.LIB_CHECKED)
+    assert not [n for n in names if not hasattr(checked, n)]
+    assert checked.grpo_device_checks() == 1 and lib.grpo_device_checks() == 0
+    P = 1 << 20
+    assert lib.grpo_selftest_bounds_check(None, None) == 1
+    assert lib.grpo_selftest_bounds_check(ctypes.c_void_p(P), None) == 7      # normal build: nothing launched
+    assert checked.grpo_selftest_bounds_check(None, None) == 1
+
+
 def test_shape_struct_layout_matches_binding(tmp_path):
     import rl_fine_tuning_gb300 as rg
     prog = tmp_path / "sz.c"
@@ -124,6 +136,7 @@ def test_status_strings_and_version(lib):
     assert rg.grpo_status_string(0) == "ok"
     assert "workspace" in rg.grpo_status_string(3)
     assert "timed out" in rg.grpo_status_string(6)
+    assert "index check" in rg.grpo_status_string(8)
     assert rg.grpo_version() >= 100
     assert rg.grpo_kernel_launches() == 0 or rg.grpo_kernel_launches() > 0
 
