@@ -140,6 +140,18 @@ def test_fwd_bwd_ragged_multi_tile_multi_chunk():
     assert_grad_parity(res, exp)
 
 
+@pytest.mark.parametrize("chunk_rows", [128, 384, 640, 1152])
+def test_chunk_heights_with_odd_tile_counts(chunk_rows):
+    # 1, 3, 5 and 9 tiles per chunk: dH's last SM pair gets a phantom tile, and the
+    # last chunk is partial (N_valid is not a multiple of the chunk height)
+    cfg = synth.make_config("tiny", G=4, L=700, d=192, V=1500, len_lo=100, len_hi=700)
+    _, dw, res, exp = _run(cfg, seed=13, chunk_rows=chunk_rows)
+    assert rg.grpo_chunk_rows(dw.shape) == chunk_rows
+    assert int(exp["mask"].sum()) % chunk_rows != 0
+    assert_fwd_parity(res, exp)
+    assert_grad_parity(res, exp)
+
+
 def test_fwd_bwd_scattered_mask():
     cfg = synth.make_config("tiny", G=2, L=200, d=128, V=777)
     rng = np.random.default_rng(5)
