@@ -334,7 +334,6 @@ def run_ours(args, ranks):
     ranks.barrier()
     torch.cuda.synchronize()
     sampler = ClockSampler(gpu_uuid())
-    rg.grpo_profile_enable(True)
     launches0 = rg.grpo_kernel_launches()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -343,12 +342,19 @@ def run_ours(args, ranks):
         step(dev)
     e1.record(stream)
     torch.cuda.synchronize()
-    rg.grpo_profile_enable(False)
     launches = rg.grpo_kernel_launches() - launches0
-    prof = rg.grpo_profile_collect()
     clocks = sampler.stop()
     ranks.barrier()
     ms = e0.elapsed_time(e1)
+    # the per-kernel breakdown comes from a second pass over the same steps with
+    # the library's launch events on (they cost about 1% of the step, so they
+    # stay out of the timed region above)
+    rg.grpo_profile_enable(True)
+    for _ in range(args.steps):
+        step(dev)
+    torch.cuda.synchronize()
+    rg.grpo_profile_enable(False)
+    prof = rg.grpo_profile_collect()
     ms_max = ranks.max(ms)
     peak_extra = torch.cuda.max_memory_allocated() - mem_base
     ms_step = ms_max / args.steps
