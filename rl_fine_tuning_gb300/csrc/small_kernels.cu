@@ -1,5 +1,7 @@
-// Bandwidth-light steps of the GRPO loss: advantages, mask / row index,
-// logsumexp merge + objective + deterministic loss, row gather and zeroing.
+// The steps of the GRPO loss that are not GEMMs: advantages, mask / row
+// index, logsumexp merge + objective + deterministic loss, row gather, the
+// dlogits pass over the kept exponentials (HBM-bound), zeroing, and the
+// self-test of the checked build.
 #include <cfloat>
 #include <cmath>
 #include <cuda_bf16.h>

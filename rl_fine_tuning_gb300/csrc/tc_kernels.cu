@@ -1,25 +1,34 @@
 // Tensor-core kernels of the linear GRPO loss (tcgen05 + TMEM, fed by TMA).
 //
-//   fwd : z = H . W^T for the policy and the reference rows of one row tile,
-//         both MMAs reading the same W stage; the epilogue keeps a running
+// SM-pair kernels (tcgen05.mma.cta_group::2, M = 256: one 128-row A tile per
+// CTA, the 256-wide B tile split between them), one backward chunk per launch:
+//   grpo_fwd_pair_kernel  z = H . W^T for the chunk's policy rows (leader CTA)
+//         and reference rows (peer CTA) of one 128-row tile, both halves of
+//         the MMA reading the same W stage; the epilogue keeps a running
 //         (max, sum exp) per row and picks out z[tok] -- the logits are never
 //         written anywhere ("Long-context GRPO", section 2: the linear
-//         algorithm; section 4: the logsumexp trick).
-//   ds  : recomputes the policy logits of a chunk of valid rows and writes
-//         the scaled dlogits  s * g_t * (onehot(tok_t) - softmax(z_t))  as
-//         16-bit values into the chunk buffer.
-//   dh  : dH[rows] = (1/N_valid) * dlogits . W        (K = vocabulary)
-//   dw  : dW      += (1/N_valid) * dlogits^T . H_pol  (K = chunk rows)
+//         algorithm; section 4: the logsumexp trick).  When a backward
+//         follows, the leader also keeps exp(z - running max) in bf16 and the
+//         running max per 32 columns, which a streaming pass later turns into
+//         the dlogits  s * g_t * (onehot(tok_t) - softmax(z_t)).
+//   grpo_fwd_pair_e4m3_kernel, grpo_fwd_pair_e5m2_kernel  the same forward
+//         on 8-bit inputs (kind::f8f6f4), scaled by the per-tensor scales.
+//   grpo_dh_pair_kernel   dH[rows] = (1/N_valid) * dlogits . W        (K = vocabulary)
+//   grpo_dw_pair_kernel   dW      += (1/N_valid) * dlogits^T . H_pol  (K = chunk rows)
+// Single-SM kernel (tcgen05.mma.cta_group::1, M = 128):
+//   grpo_fwd_lse_kernel   the forward over row tiles of h_pol / h_ref (the
+//         workspace-free entry point), policy and reference MMAs sharing B.
 //
 // One persistent CTA per SM, 6 warps:
 //   warp 0      TMA producer (one lane)
-//   warp 1      TMEM allocator + MMA issuer (one lane)
+//   warp 1      TMEM allocator + MMA issuer (one lane; in a pair, the leader's)
 //   warps 2..5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31,
 //               i.e. one accumulator row per thread.
 // Stages: smem ring of kStages K-slices (64 elements = one 128-byte swizzle
-// span), full/empty mbarriers; accumulators: kAccBufs TMEM buffers with
-// acc_full/acc_empty mbarriers so the epilogue of one tile overlaps the MMAs
-// of the next.
+// span), full/empty mbarriers; accumulators: double-buffered in TMEM (except
+// the single-SM forward, whose two accumulators are the policy and reference
+// tiles) with acc_full/acc_empty mbarriers, so the epilogue of one tile
+// overlaps the MMAs of the next.
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
