@@ -477,14 +477,20 @@ def run_ours(args, ranks):
             ent["gbs"] = bytes_kind[k] * args.steps / (kms / 1e3) / 1e9
         kernels[k] = ent
     dom = max(flops_kind, key=lambda k: prof[k][0])
-    dom_ms, dom_n = prof[dom]
+    R = rg.grpo_chunk_rows(shape)
+    n_chunks_work = (n_valid + R - 1) // R
+    dom_ms, _ = prof[dom]
     sustained = pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     achieved = flops_kind[dom] * args.steps / (dom_ms / 1e3) / 1e12
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                 "frac": achieved / sustained, "peak_kind": f"bf16 dense sustained, {pk_kind}",
                 "traffic": ncu_traffic(dom, rg.grpo_chunk_rows(shape)),
                 "traffic_per": "full chunk launch (ncu DRAM read+write bytes)",
-                "flops_per_launch": flops_kind[dom] * args.steps / dom_n, "ms_per_launch": dom_ms / dom_n}
+                # per full chunk of R rows, like traffic: its algorithmic flops, and the kernel's
+                # time per R rows (empty chunk slots exit at once and add nothing)
+                "rows_per_launch": R, "launches_with_rows": n_chunks_work,
+                "flops_per_launch": flops_kind[dom] / n_valid * R,
+                "ms_per_launch": dom_ms / args.steps / n_valid * R}
     useful = 8.0 * n_valid * V * d
     t_step = ms_step / 1e3
     burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
