@@ -167,6 +167,8 @@ def test_fwd_bwd_scattered_mask():
     dict(G=1, sigma_ref=0.3),                                # one completion: A = 0, only the KL term acts
     dict(G=2, L=100, d=64, V=257 * 256, len_lo=40, len_hi=100),   # 257 vocabulary tiles: no even split exists
     dict(G=2, L=160, d=8192, V=600, len_lo=60, len_hi=160),      # d of a 70B-class head: 32 d tiles, K = 128 stages
+    dict(w_sigma=2.0),                                       # logits up to ~110: near one-hot softmax
+    dict(w_sigma=6.0),                                       # logits up to ~330, p - q of order 10
 ])
 def test_degenerate_shapes(over):
     cfg = synth.make_config("tiny", **over)
