@@ -27,6 +27,12 @@
  *   - The variants of the four-way experiment of the same section and a
  *     per-completion mean; the pages give no formulas for these (their
  *     images are lost), so they follow the readings stated at each function.
+ *     The three objective variants (no detach, reverse KL times Q, forward
+ *     KL) are parity unpinned against the pages: the tests pin each one's
+ *     gradient to its own value by finite differences, but nothing on the
+ *     pages fixes the values themselves.
+ *   - Exact decoders of the OCP FP8 formats E4M3 and E5M2 (the 8-bit forward
+ *     reads its inputs as code * scale).
  *
  * Everything is fp64 on inputs widened exactly from their storage type
  * (bf16 / fp16 / double).  Sums run in ascending index order.  OpenMP only
