@@ -211,15 +211,6 @@ def oracle_sample(cfg, wl, rows, adv):
     return time.perf_counter() - t0
 
 
-def oracle_rows_for(cfg, seconds, per_row_s=None):
-    # about 6*V*d fp64 multiply-adds per row; assume ~0.5 GMAC/s per host thread until measured
-    import oracle
-    thr = max(1, oracle.max_threads())
-    if per_row_s is None:
-        per_row_s = 6.0 * cfg.V * cfg.d / (0.5e9 * thr)
-    return max(thr, int(seconds / per_row_s))
-
-
 # --------------------------------------------------------------------------- reference arm
 
 def run_reference(args, ranks):
