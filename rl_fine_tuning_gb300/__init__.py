@@ -15,10 +15,12 @@ import os
 from . import build as _build
 
 __all__ = [
-    "GrpoError", "GrpoShape", "BF16", "FP16", "load", "make_shape", "grpo_workspace_bytes",
-    "grpo_group_advantages", "grpo_build_mask", "grpo_valid_rows", "grpo_loss_fwd", "grpo_loss_fwd_bwd",
+    "GrpoError", "GrpoShape", "BF16", "FP16", "E4M3", "E5M2", "TOKEN_MEAN", "SEQUENCE_MEAN", "OBJECTIVES", "load",
+    "make_shape", "grpo_workspace_bytes", "grpo_chunk_rows", "grpo_group_advantages", "grpo_build_mask",
+    "grpo_valid_rows", "grpo_loss_fwd", "grpo_loss_fwd_bwd", "grpo_loss_fwd_fp8", "grpo_loss_fwd_noalloc",
     "grpo_status_string", "grpo_version", "library_path", "grpo_profile_enable", "grpo_profile_collect",
-    "grpo_kernel_launches", "PROF_KINDS",
+    "grpo_kernel_launches", "grpo_device_checks", "grpo_selftest_bounds_check", "grpo_selftest_wait_timeout",
+    "PROF_KINDS",
 ]
 
 # kernel kinds of the diagnostics interface, in the order of the GRPO_PROF_* enum
@@ -67,31 +69,39 @@ def load(build_if_missing: bool = False):
     if not os.path.exists(path):
         raise ImportError(f"libgrpo.so is not built ({path}); run `python -m rl_fine_tuning_gb300.build`")
     lib = ctypes.CDLL(path)
-    p, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
-    sp = ctypes.POINTER(GrpoShape)
-    lib.grpo_shape_init.argtypes = [sp, i32, i32, i32, i32, i32, i32]
-    lib.grpo_shape_init.restype = None
-    lib.grpo_workspace_bytes.argtypes = [sp]
-    lib.grpo_workspace_bytes.restype = sz
-    lib.grpo_group_advantages.argtypes = [p, i32, i32, f32, i32, p, p]
-    lib.grpo_build_mask.argtypes = [p, sp, p, p]
-    lib.grpo_valid_rows.argtypes = [p, sp, p, p, p, sz, p]
-    lib.grpo_loss_fwd.argtypes = [p, p, p, p, p, p, sp, p, sz, p, p, p, p]
-    lib.grpo_loss_fwd_bwd.argtypes = [p, p, p, p, p, p, sp, f32, p, sz, p, p, p, p, p, p, p]
-    lib.grpo_status_string.argtypes = [i32]
-    lib.grpo_status_string.restype = ctypes.c_char_p
-    lib.grpo_version.restype = i32
-    lib.grpo_profile_enable.argtypes = [i32]
-    lib.grpo_profile_enable.restype = i32
-    lib.grpo_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), i32]
-    lib.grpo_profile_collect.restype = i32
-    lib.grpo_kernel_launches.argtypes = []
-    lib.grpo_kernel_launches.restype = ctypes.c_ulonglong
-    for name in ("grpo_group_advantages", "grpo_build_mask", "grpo_valid_rows", "grpo_loss_fwd",
-                 "grpo_loss_fwd_bwd"):
-        getattr(lib, name).restype = i32
+    _declare(lib)
     _lib = lib
     return lib
+
+
+def _declare(lib):
+    """Argument and result types of every entry point of include/grpo.h."""
+    p, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+    sp = ctypes.POINTER(GrpoShape)
+    sigs = {
+        "grpo_shape_init": ([sp, i32, i32, i32, i32, i32, i32], None),
+        "grpo_workspace_bytes": ([sp], sz),
+        "grpo_chunk_rows": ([sp], i32),
+        "grpo_group_advantages": ([p, i32, i32, f32, i32, p, p], i32),
+        "grpo_build_mask": ([p, sp, p, p], i32),
+        "grpo_valid_rows": ([p, sp, p, p, p, sz, p], i32),
+        "grpo_loss_fwd": ([p, p, p, p, p, p, sp, p, sz, p, p, p, p], i32),
+        "grpo_loss_fwd_bwd": ([p, p, p, p, p, p, sp, f32, p, sz, p, p, p, p, p, p, p], i32),
+        "grpo_loss_fwd_fp8": ([p, p, p, f32, f32, f32, p, p, p, sp, p, sz, p, p, p, p], i32),
+        "grpo_loss_fwd_noalloc": ([p, p, p, p, p, p, sp, p, p, p, p], i32),
+        "grpo_profile_enable": ([i32], i32),
+        "grpo_profile_collect": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), i32], i32),
+        "grpo_kernel_launches": ([], ctypes.c_ulonglong),
+        "grpo_device_checks": ([], i32),
+        "grpo_selftest_bounds_check": ([p, p], i32),
+        "grpo_selftest_wait_timeout": ([p, p, p], i32),
+        "grpo_status_string": ([i32], ctypes.c_char_p),
+        "grpo_version": ([], i32),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
 
 
 def _status_string(code: int) -> str:
@@ -202,25 +212,17 @@ def grpo_kernel_launches() -> int:
 
 def grpo_loss_fwd_noalloc(h_pol, h_ref, W, tokens, mask, adv, shape, loss_out, row_stats, status, stream=None):
     """grpo_loss_fwd on the library's own fixed scratch array (no workspace argument)."""
-    fn = load().grpo_loss_fwd_noalloc
-    if fn.argtypes is None:
-        p = ctypes.c_void_p
-        fn.argtypes = [p, p, p, p, p, p, ctypes.POINTER(GrpoShape), p, p, p, p]
-        fn.restype = ctypes.c_int
-    _check(fn(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv), ctypes.byref(shape),
-              _ptr(loss_out), _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_noalloc")
+    _check(load().grpo_loss_fwd_noalloc(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv),
+                                        ctypes.byref(shape), _ptr(loss_out), _ptr(row_stats), _ptr(status),
+                                        _stream(stream)), "grpo_loss_fwd_noalloc")
 
 
 def grpo_loss_fwd_fp8(h_pol, h_ref, W, scale_h_pol, scale_h_ref, scale_w, tokens, mask, adv, shape, workspace,
                       loss_out, row_stats, status, stream=None):
-    fn = load().grpo_loss_fwd_fp8
-    if fn.argtypes is None:
-        p, f = ctypes.c_void_p, ctypes.c_float
-        fn.argtypes = [p, p, p, f, f, f, p, p, p, ctypes.POINTER(GrpoShape), p, ctypes.c_size_t, p, p, p, p]
-        fn.restype = ctypes.c_int
-    _check(fn(_ptr(h_pol), _ptr(h_ref), _ptr(W), float(scale_h_pol), float(scale_h_ref), float(scale_w), _ptr(tokens),
-              _ptr(mask), _ptr(adv), ctypes.byref(shape), _ptr(workspace), _nbytes(workspace), _ptr(loss_out),
-              _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_fp8")
+    _check(load().grpo_loss_fwd_fp8(_ptr(h_pol), _ptr(h_ref), _ptr(W), float(scale_h_pol), float(scale_h_ref),
+                                    float(scale_w), _ptr(tokens), _ptr(mask), _ptr(adv), ctypes.byref(shape),
+                                    _ptr(workspace), _nbytes(workspace), _ptr(loss_out), _ptr(row_stats),
+                                    _ptr(status), _stream(stream)), "grpo_loss_fwd_fp8")
 
 
 def grpo_device_checks() -> bool:
@@ -229,16 +231,9 @@ def grpo_device_checks() -> bool:
 
 
 def grpo_selftest_bounds_check(status, stream=None):
-    fn = load().grpo_selftest_bounds_check
-    if fn.argtypes is None:
-        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
-        fn.restype = ctypes.c_int
-    _check(fn(_ptr(status), _stream(stream)), "grpo_selftest_bounds_check")
+    _check(load().grpo_selftest_bounds_check(_ptr(status), _stream(stream)), "grpo_selftest_bounds_check")
 
 
 def grpo_selftest_wait_timeout(status, waited_ns, stream=None):
-    fn = load().grpo_selftest_wait_timeout
-    if fn.argtypes is None:
-        fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
-        fn.restype = ctypes.c_int
-    _check(fn(_ptr(status), _ptr(waited_ns), _stream(stream)), "grpo_selftest_wait_timeout")
+    _check(load().grpo_selftest_wait_timeout(_ptr(status), _ptr(waited_ns), _stream(stream)),
+           "grpo_selftest_wait_timeout")

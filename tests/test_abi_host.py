@@ -36,6 +36,25 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= exported
 
 
+def declared_parameter_counts():
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    counts = {}
+    for name, params in re.findall(r"\b(grpo_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", src):
+        params = params.strip()
+        counts[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_declares_every_entry_point_with_the_header_arity(lib):
+    counts = declared_parameter_counts()
+    assert set(counts) == set(declared_functions())
+    for name, n in counts.items():
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
 def test_checked_build_exports_the_same_symbols_and_says_so(lib):
     from rl_fine_tuning_gb300 import build
     names = declared_functions()
