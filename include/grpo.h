@@ -33,6 +33,9 @@
  *   - Row t = i*L + j is position j of completion i; completion i belongs to
  *     prompt group i / G.  N = n_groups * G * L.
  *   - All hidden-state rows, masked or not, must hold finite values.
+ *   - Several host threads may call the entry points at once, each call with
+ *     its own workspace and outputs.  grpo_loss_fwd_noalloc is the exception
+ *     (its calls share one array; see there).
  *   - Nothing throws, aborts or exits the process.
  */
 #ifndef GRPO_H
@@ -231,9 +234,11 @@ int grpo_loss_fwd_noalloc(const void* h_pol, const void* h_ref, const void* W, c
  * grpo_profile_collect waits for the recorded events, adds the elapsed
  * milliseconds of each kernel kind into ms[kind] and the launch count into
  * launches[kind] (arrays of at least GRPO_PROF_KINDS entries, caller-owned
- * host memory), and clears the records.  Not thread-safe; meant for
- * benchmarks.  grpo_kernel_launches counts every kernel launched by the
- * library since it was loaded, profiling on or off. */
+ * host memory), and clears the records.  Meant for benchmarks: the
+ * records of every thread's launches go into one list, and while profiling
+ * is on, launches from different threads take turns on a lock.
+ * grpo_kernel_launches counts every kernel launched by the library since it
+ * was loaded, profiling on or off. */
 enum {
     GRPO_PROF_ADVANTAGES = 0,
     GRPO_PROF_MASK,

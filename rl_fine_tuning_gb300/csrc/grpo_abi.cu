@@ -25,8 +25,11 @@ struct ProfRecord {
     cudaEvent_t a, b;
 };
 
+// `on` is read by every launch; the records and the event pool are touched
+// only while profiling is on, under `mu`.
 struct Profiler {
-    bool on = false;
+    std::atomic<bool> on{false};
+    std::mutex mu;
     std::vector<ProfRecord> recs;
     std::vector<cudaEvent_t> pool;
     cudaEvent_t get() {
@@ -45,15 +48,17 @@ Profiler g_prof;
 // launch one kernel through `fn`, counting it and timing it when profiling is on
 template <class F>
 cudaError_t launch(int kind, cudaStream_t st, F&& fn) {
-    cudaEvent_t a = nullptr, b = nullptr;
-    if (g_prof.on) {
-        a = g_prof.get();
-        b = g_prof.get();
-        if (a) cudaEventRecord(a, st);
+    if (!g_prof.on.load(std::memory_order_relaxed)) {
+        const cudaError_t e = fn();
+        if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+        return e;
     }
-    cudaError_t e = fn();
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    cudaEvent_t a = g_prof.get(), b = g_prof.get();
+    if (a) cudaEventRecord(a, st);
+    const cudaError_t e = fn();
     if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (g_prof.on && a && b) {
+    if (a && b) {
         cudaEventRecord(b, st);
         g_prof.recs.push_back(ProfRecord{kind, a, b});
     }
@@ -101,16 +106,17 @@ int device_info(DeviceInfo* out) {
     return GRPO_OK;
 }
 
+// looked up once per process (a thread-safe static initialisation)
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
     return fn;
 }
 
@@ -681,12 +687,13 @@ const char* grpo_status_string(int status) {
 int grpo_version(void) { return kVersion; }
 
 int grpo_profile_enable(int on) {
-    g_prof.on = on != 0;
+    g_prof.on.store(on != 0);
     return GRPO_OK;
 }
 
 int grpo_profile_collect(double* ms, long long* launches, int n_kinds) {
     if ((!ms || !launches) && n_kinds > 0) return GRPO_ERR_POINTER;
+    std::lock_guard<std::mutex> lock(g_prof.mu);
     int rc = GRPO_OK;
     for (const ProfRecord& r : g_prof.recs) {
         float t = 0.f;

@@ -59,3 +59,57 @@ def test_concurrent_calls_on_two_streams_match_sequential():
         torch.cuda.synchronize()
         assert _same(_snapshot(a), seq_a)
         assert _same(_snapshot(b), seq_b)
+
+
+def test_calls_from_two_host_threads_match_sequential():
+    """Two host threads call the library at once (ctypes releases the GIL for
+    the call), with per-kernel profiling on: the same bits as sequential
+    calls, and the profiler counts every launch of both threads once."""
+    import threading
+
+    cfg_a = synth.make_config("tiny", G=2, L=300, d=192, V=900, len_lo=1, len_hi=300)
+    cfg_b = synth.make_config("tiny", G=4, L=128, d=128, V=1300, sigma_ref=0.2)
+    a = DeviceWorkload(synth.generate(cfg_a, seed=41), chunk_rows=128)
+    b = DeviceWorkload(synth.generate(cfg_b, seed=42), chunk_rows=256)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    reps = 4
+
+    rg.grpo_profile_enable(True)
+    try:
+        rg.grpo_profile_collect()
+        _call(a, s1)
+        _call(b, s1)
+        s1.synchronize()
+        once = rg.grpo_profile_collect()
+        seq_a, seq_b = _snapshot(a), _snapshot(b)
+        assert int(seq_a[-1].item()) == 0 and int(seq_b[-1].item()) == 0
+
+        errors = []
+        start = threading.Barrier(2)
+
+        def worker(dw, stream):
+            try:
+                torch.cuda.set_device(0)
+                start.wait(timeout=60)
+                for _ in range(reps):
+                    _call(dw, stream)
+            except Exception as e:   # re-raised in the main thread
+                errors.append(e)
+
+        threads = [threading.Thread(target=worker, args=(a, s1)), threading.Thread(target=worker, args=(b, s2))]
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        torch.cuda.synchronize()
+        assert not errors, errors
+        prof = rg.grpo_profile_collect()
+    finally:
+        rg.grpo_profile_enable(False)
+        rg.grpo_profile_collect()
+    assert _same(_snapshot(a), seq_a)
+    assert _same(_snapshot(b), seq_b)
+    for kind, (_, n) in once.items():
+        assert prof[kind][1] == reps * n, (kind, prof[kind][1], n)
