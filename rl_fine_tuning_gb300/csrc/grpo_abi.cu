@@ -404,16 +404,18 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     // masked rows: objective 0; with a backward: found_inf <- 0, dW <- 0 when no row
     // is masked in, dH rows of masked rows <- 0
     if (launch(GRPO_PROF_CLEAR, st, [&] {
-            return launch_rows_init(in.mask, L.N, reinterpret_cast<float*>(w + L.ell), in.row_stats, st);
+            return launch_rows_init(in.mask, L.N, reinterpret_cast<float*>(w + L.ell), in.row_stats, dev.sm_count, st);
         }) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
     if (bwd) {
         if (launch(GRPO_PROF_CLEAR, st, [&] {
-                return launch_clear_grads(counts, bwd->found_inf, bwd->dW, static_cast<int64_t>(s.V) * s.d, st);
+                return launch_clear_grads(counts, bwd->found_inf, bwd->dW, static_cast<int64_t>(s.V) * s.d,
+                                          dev.sm_count, st);
             }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_CLEAR, st, [&] { return launch_zero_masked_rows(in.mask, L.N, s.d, bwd->dH, st); }) !=
-            cudaSuccess)
+        if (launch(GRPO_PROF_CLEAR, st, [&] {
+                return launch_zero_masked_rows(in.mask, L.N, s.d, bwd->dH, dev.sm_count, st);
+            }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
     }
 
@@ -479,9 +481,9 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         fp.chunk = ci;
         fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
         const MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
-        if (launch(GRPO_PROF_GATHER, st,
-                   [&] { return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, row_bytes, st); }) !=
-            cudaSuccess)
+        if (launch(GRPO_PROF_GATHER, st, [&] {
+                return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, row_bytes, dev.sm_count, st);
+            }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_FWD, st, [&] {
                 return f8 ? launch_fwd_pair_fp8(fp, mHc_k, mHcr_k, mW_k, dev.sm_count, f8->e5m2, st)
@@ -490,7 +492,8 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
         if (!bwd) continue;
-        if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, st); }) != cudaSuccess)
+        if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, dev.sm_count, st); }) !=
+            cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
             cudaSuccess)

@@ -147,14 +147,16 @@ cudaError_t launch_advantages(const float* r, int n_groups, int G, float eps, in
 cudaError_t launch_build_mask(const int32_t* lengths, int n_seq, int L, uint8_t* mask, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_seq_counts(const uint8_t* mask, int n_seq, int L, int* seqcnt, int* counts, cudaStream_t st);
-cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, cudaStream_t st);
+cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, int sm_count,
+                             cudaStream_t st);
 cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, int nblk, const int* counts,
                                float* loss_out, cudaStream_t st);
+// The grid-stride kernels below size their grids in multiples of the device's SM count.
 cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
-                               int row_bytes, cudaStream_t st);
-cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, cudaStream_t st);
-cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, cudaStream_t st);
-cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st);
+                               int row_bytes, int sm_count, cudaStream_t st);
+cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, int sm_count, cudaStream_t st);
+cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, int sm_count, cudaStream_t st);
+cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, int sm_count, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cudaStream_t st);
 #ifdef GRPO_DEVICE_CHECKS

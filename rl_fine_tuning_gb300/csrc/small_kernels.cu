@@ -400,9 +400,10 @@ __global__ void k_rows_init(const uint8_t* __restrict__ mask, int64_t N, float* 
     }
 }
 
-cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, cudaStream_t st) {
+cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, int sm_count,
+                             cudaStream_t st) {
     int blocks = static_cast<int>((N + 255) / 256);
-    if (blocks > 2048) blocks = 2048;
+    if (blocks > sm_count * 8) blocks = sm_count * 8;
     if (blocks < 1) blocks = 1;
     k_rows_init<<<blocks, 256, 0, st>>>(mask, N, ell, row_stats);
     return cudaGetLastError();
@@ -496,11 +497,11 @@ cudaError_t launch_bounds_selftest(int* status, cudaStream_t st) {
 #endif
 
 cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
-                               int row_bytes, cudaStream_t st) {
+                               int row_bytes, int sm_count, cudaStream_t st) {
     const int vpr = row_bytes / 16;
     const int64_t total = static_cast<int64_t>(R) * vpr;
     int blocks = static_cast<int>((total + 255) / 256);
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks > sm_count * 16) blocks = sm_count * 16;
     k_gather_rows<<<blocks, 256, 0, st>>>(p.counts, p.rows, p.chunk, static_cast<const uint4*>(h_pol),
                                           static_cast<uint4*>(hc), static_cast<const uint4*>(h_ref),
                                           static_cast<uint4*>(hcr), vpr, R, p.N, p.status);
@@ -570,9 +571,9 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform(const ChunkPara
     if (!kBf16 && __syncthreads_or(bad) && threadIdx.x == 0) atomicOr(p.found_inf, 1);
 }
 
-cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, cudaStream_t st) {
+cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, int sm_count, cudaStream_t st) {
     int blocks = R;
-    if (blocks > 152 * 8) blocks = 152 * 8;
+    if (blocks > sm_count * 8) blocks = sm_count * 8;
     if (bf16)
         k_transform<true><<<blocks, kTransformThreads, 0, st>>>(p, R);
     else
@@ -590,11 +591,11 @@ __global__ void k_zero_masked_rows(const uint8_t* __restrict__ mask, int64_t N, 
     }
 }
 
-cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, cudaStream_t st) {
+cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, int sm_count, cudaStream_t st) {
     const int vpr = d / 8;
     const int64_t total = N * vpr;
     int blocks = static_cast<int>((total + 255) / 256);
-    if (blocks > 148 * 16) blocks = 148 * 16;
+    if (blocks > sm_count * 16) blocks = sm_count * 16;
     if (blocks < 1) blocks = 1;
     k_zero_masked_rows<<<blocks, 256, 0, st>>>(mask, N, vpr, static_cast<uint4*>(dH));
     return cudaGetLastError();
@@ -609,10 +610,11 @@ __global__ void k_clear_grads(const int* __restrict__ counts, int* found_inf, fl
         dW[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, cudaStream_t st) {
+cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, int sm_count,
+                               cudaStream_t st) {
     const int64_t n4 = n / 4;
     int blocks = static_cast<int>((n4 + 255) / 256);
-    if (blocks > 148 * 8) blocks = 148 * 8;
+    if (blocks > sm_count * 8) blocks = sm_count * 8;
     if (blocks < 1) blocks = 1;
     k_clear_grads<<<blocks, 256, 0, st>>>(counts, found_inf, reinterpret_cast<float4*>(dW), n4);
     return cudaGetLastError();
