@@ -5,12 +5,15 @@ they need the loss -- e.g. a step sharing the GPU with an inference engine
 that has reserved all free memory -- and uses a fixed 8 MiB array inside the
 library instead of a caller workspace.  These tests call it through the C ABI
 twice in a row (the array keeps the previous call's contents) and compare it
-with grpo_loss_fwd, the entry point that takes a workspace.  The file sorts
-last so that a run stopping at the first failure has run everything else.
+with grpo_loss_fwd, the entry point that takes a workspace; and they compare
+it with the fp64 oracle for every objective variant under both means, and for
+fp16 inputs with a scattered mask.  The file sorts last so that a run
+stopping at the first failure has run everything else.
 """
 import numpy as np
 import pytest
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -21,6 +24,7 @@ if not torch.cuda.is_available():
 
 import rl_fine_tuning_gb300 as rg  # noqa: E402
 from gpu_harness import DeviceWorkload  # noqa: E402
+from test_gpu_parity import assert_fwd_parity  # noqa: E402
 
 LOSS_RTOL = 1e-3
 STAT_TOL = 1e-3
@@ -53,6 +57,34 @@ def test_noalloc_matches_workspace_forward_twice(name, over, seed):
         assert abs(got - ref_loss) <= LOSS_RTOL * max(abs(ref_loss), 1e-30), (call, got, ref_loss)
         s = stats.cpu().numpy()
         assert np.all(np.abs(s - ref_stats) <= STAT_TOL * np.maximum(1.0, np.abs(ref_stats))), call
+
+
+def _noalloc_against_oracle(cfg, seed, mask=None, objective=0, loss_mode=0):
+    wl = synth.generate(cfg, seed=seed)
+    dw = DeviceWorkload(wl, mask=mask, objective=objective, loss_mode=loss_mode)
+    dw.loss.fill_(float("nan"))
+    dw.status.fill_(-1)
+    _noalloc(dw, dw.loss, dw.row_stats, dw.status)
+    res = dw.results()
+    exp = oracle.expected(wl, mask=res["mask"], want_dH=False, want_dW=False, objective=objective,
+                          loss_mode=loss_mode)
+    assert_fwd_parity(res, exp)
+
+
+@pytest.mark.parametrize("objective", ["grpo", "no_detach", "reverse_kl_q", "forward_kl"])
+@pytest.mark.parametrize("loss_mode", [0, 1])
+def test_noalloc_objectives_and_means_against_oracle(objective, loss_mode):
+    # three prompt groups, one completion fully masked, a KL large enough to matter
+    cfg = synth.make_config("tiny", n_groups=3, G=4, L=150, d=192, V=1000, len_lo=1, len_hi=150,
+                            n_zero_seq=1, sigma_ref=0.3)
+    _noalloc_against_oracle(cfg, 43, objective=objective, loss_mode=loss_mode)
+
+
+def test_noalloc_fp16_scattered_mask_against_oracle():
+    # fp16 inputs, ragged V and d, a mask that is not a prefix of each completion
+    cfg = synth.make_config("tiny", dtype="fp16", G=4, L=200, d=320, V=777, sigma_ref=0.1)
+    mask = (np.random.default_rng(47).random(cfg.N) < 0.45).astype(np.uint8)
+    _noalloc_against_oracle(cfg, 47, mask=mask)
 
 
 def test_noalloc_rejects_shapes_beyond_its_array():
