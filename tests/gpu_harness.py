@@ -61,8 +61,9 @@ class DeviceWorkload:
         self.found_inf = t.zeros(1, dtype=t.int32, device="cuda")
         self.row_stats = t.zeros((cfg.N, 5), dtype=t.float32, device="cuda")
         dt = t.bfloat16 if cfg.dtype == "bf16" else t.float16
-        self.dH = t.empty((cfg.N, cfg.d), dtype=dt, device="cuda")
-        self.dW = t.empty((cfg.V, cfg.d), dtype=t.float32, device="cuda")
+        # a finite sentinel: a backward must overwrite every element (masked dH rows with 0)
+        self.dH = t.full((cfg.N, cfg.d), 7.0, dtype=dt, device="cuda")
+        self.dW = t.full((cfg.V, cfg.d), 7.0, dtype=t.float32, device="cuda")
 
     def fwd(self):
         rg.grpo_loss_fwd(self.h_pol, self.h_ref, self.W, self.tokens, self.mask, self.adv, self.shape, self.ws,
