@@ -99,6 +99,7 @@ class ClockSampler:
     def __init__(self, gpu_uuid=None):
         self.proc = None
         self.path = None
+        self.out = None
         try:
             import tempfile
             fd, self.path = tempfile.mkstemp(prefix="grpo_clocks_", suffix=".csv")
@@ -110,9 +111,20 @@ class ClockSampler:
             self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            self._discard()
+
+    def _discard(self):
+        """Close and remove the sample file (no sampler is running)."""
+        if self.out is not None:
+            self.out.close()
+            self.out = None
+        if self.path and os.path.exists(self.path):
+            os.unlink(self.path)
+        self.path = None
 
     def stop(self):
         if not self.proc:
+            self._discard()
             return None
         self.proc.terminate()
         try:
@@ -135,6 +147,7 @@ class ClockSampler:
                     if val.lower() == "active":
                         reasons.add(name)
         os.unlink(self.path)
+        self.path = None
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),

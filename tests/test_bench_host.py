@@ -47,8 +47,29 @@ def test_clock_sampler_reports_slowdowns(tmp_path, monkeypatch):
 
 
 def test_clock_sampler_without_nvidia_smi(tmp_path, monkeypatch):
-    monkeypatch.setenv("PATH", str(tmp_path))
-    assert bench.ClockSampler().stop() is None
+    import tempfile
+    empty = tmp_path / "bin"
+    empty.mkdir()
+    scratch = tmp_path / "scratch"
+    scratch.mkdir()
+    monkeypatch.setenv("PATH", str(empty))
+    monkeypatch.setattr(tempfile, "tempdir", str(scratch))
+    s = bench.ClockSampler()
+    assert not os.listdir(scratch)          # nothing left behind when the sampler cannot start
+    assert s.stop() is None
+
+
+def test_clock_sampler_removes_its_file(tmp_path, monkeypatch):
+    import tempfile
+    scratch = tmp_path / "scratch"
+    scratch.mkdir()
+    lines = ["0, 1400, 2070, 1300, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    monkeypatch.setenv("PATH", _fake_smi(tmp_path, lines) + os.pathsep + os.environ["PATH"])
+    monkeypatch.setattr(tempfile, "tempdir", str(scratch))
+    s = bench.ClockSampler()
+    time.sleep(0.3)
+    assert s.stop()["sm_mhz"] == 1400.0
+    assert not os.listdir(scratch)
 
 
 def test_peaks_come_from_the_measured_file_or_the_fallback(tmp_path, monkeypatch):
