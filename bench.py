@@ -348,6 +348,10 @@ def run_ours(args, ranks):
     torch.cuda.synchronize()
     launches = rg.grpo_kernel_launches() - launches0
     clocks = sampler.stop()
+    # the timed steps repeat the warm-up's inputs at its settled loss scale, so
+    # none may overflow; a step that did would need a retry the timing lacks
+    if int(found_inf.item()) != 0 or int(status.item()) != 0:
+        raise SystemExit("a timed step overflowed or reported a device error")
     ranks.barrier()
     ms = e0.elapsed_time(e1)
     # the per-kernel breakdown comes from a second pass over the same steps with
