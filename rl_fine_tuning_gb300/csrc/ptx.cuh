@@ -72,6 +72,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// After an abort, TMA loads that the CTA issued before its roles stopped may
+// still be writing into its shared memory.  In a CTA pair they complete on the
+// leader's barrier, which the issuing peer cannot observe, so the CTA cannot
+// wait for them one by one.  An issued load lands within microseconds: every
+// thread of an aborting CTA waits this long before the CTA leaves.
+constexpr unsigned long long kAbortGraceNs = 200ull * 1000ull;   // 200 us
+
+// Call after the CTA's last __syncthreads, when the flag no longer changes.
+__device__ __forceinline__ void abort_grace(const volatile int* abort_flag) {
+    if (!*abort_flag) return;
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < kAbortGraceNs) {
+    }
+}
+
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -455,6 +455,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    abort_grace(sm.abort_flag);
     // peers may still multicast into this CTA's shared memory until they are done
     if (kC > 1) cluster_sync();
     if (warp == 1) {
@@ -1015,6 +1016,7 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    abort_grace(sm.abort_flag);
     // the leader's MMAs write the peer's tensor memory, and the peer's loads
     // complete on the leader's barriers: nobody leaves before both are done
     cluster_sync();
