@@ -5,7 +5,8 @@
 
 One step = the whole hot path on one batch: group advantages, completion
 mask, row index, policy+reference lm_head logits with streaming logsumexp,
-objective and masked mean, and the recompute backward to dH and dW.  The
+objective and masked mean, and the backward: dlogits from the exponentials
+the forward kept, then dH and dW.  The
 default workload is the Llama-3.1-8B head at 20K context with 8 completions
 (G=8, L=20000, d=4096, V=128256, bf16), synthetic seeded inputs shaped like
 the pages' long-context run.  Inputs (W 1 GB, hidden states 1.3 GB each) are

@@ -358,7 +358,7 @@ int run_forward(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     CUtensorMap mHp, mHr, mW;
     if (!make_map(&mHp, in.h_pol, bf16, s.d, L.N, s.d, kBK, kBM) ||
         !make_map(&mHr, in.h_ref, bf16, s.d, L.N, s.d, kBK, kBM) ||
-        !make_map(&mW, in.W, bf16, s.d, s.V, s.d, kBK, kBN / kClusterFwd))
+        !make_map(&mW, in.W, bf16, s.d, s.V, s.d, kBK, kBN))
         return GRPO_ERR_LAUNCH;
     FwdParams fp = fwd_params(in, L, w);
     fp.tiles = reinterpret_cast<const int2*>(w + L.tiles);
@@ -722,8 +722,8 @@ unsigned long long grpo_kernel_launches(void) { return g_launches.load(); }
 //
 // Some callers cannot allocate device memory when they need the loss: a
 // training step that runs next to an inference engine which has reserved all
-// free device memory for its own pool (the pages describe sharing one CUDA
-// memory space with vLLM), or code that must not pay for cudaMalloc's
+// free device memory for its own pool ("Long-context GRPO", section 2 (3):
+// training and vLLM inference share one memory space), or code that must not pay for cudaMalloc's
 // device-wide synchronisation inside its step.  This entry point serves them
 // from a fixed array that lives in the library itself.
 namespace {

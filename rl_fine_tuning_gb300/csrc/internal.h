@@ -43,8 +43,6 @@ constexpr int kChunkTilesLarge = 76;
 constexpr int kMergeThreads = 256;
 constexpr int kIndexThreads = 1024;
 constexpr int kTransformThreads = 256;
-// CTAs per cluster of the forward-only kernel (clusters share each W tile through TMA multicast)
-constexpr int kClusterFwd = 1;
 
 // int32 words at the start of the workspace
 enum CountSlot {

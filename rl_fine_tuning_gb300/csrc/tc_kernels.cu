@@ -109,13 +109,6 @@ __device__ __forceinline__ bool half2_nonfinite(uint32_t u) {
 // ====================================================================== traits
 // Each traits class describes one kernel: its schedule of work units, the TMA
 // loads of one K-stage, the MMAs of one K-stage and the epilogue.
-//
-// Work is handed out per cluster of C CTAs (C = 1, 2 or 4).  The C CTAs of a
-// cluster compute C different 128-row M tiles against the SAME 256-wide B
-// tile: each CTA loads its own A tile and 1/C of the B tile, multicasting its
-// slice to every CTA of the cluster, so L2 serves each B tile once per
-// cluster.  A CTA whose M tile lies past the end ("phantom") still loads and
-// multicasts its B slice and runs its MMAs, but its epilogue writes nothing.
 
 struct FwdT {
     static constexpr int kStages = 3;
@@ -124,7 +117,7 @@ struct FwdT {
     static constexpr int kAccStride = 0;
     using Params = FwdParams;
     struct Sched {
-        int n_units, ks, n_tiles, C;
+        int n_units, ks, n_tiles;
     };
     struct Coord {
         int t0, n0;
@@ -135,18 +128,15 @@ struct FwdT {
         bool valid, found;
     };
 
-    // unit = tile group * S + split; the tile of rank r is group * C + r.  Tiles
-    // are the forward row tiles over h_pol/h_ref (runs of masked-in rows).
-    __device__ static bool setup(const Params& p, Sched& sc, int C) {
-        sc.C = C;
+    // unit = tile * S + split.  Tiles are the forward row tiles over
+    // h_pol/h_ref (runs of masked-in rows).
+    __device__ static bool setup(const Params& p, Sched& sc) {
         sc.n_tiles = p.counts[C_NTILES];
-        sc.n_units = ((sc.n_tiles + C - 1) / C) * p.S;
+        sc.n_units = sc.n_tiles * p.S;
         sc.ks = p.d / kBK;
         return sc.n_units > 0;
     }
-    __device__ static int tile_of(const Params& p, const Sched& sc, int unit, int rank) {
-        return (unit / p.S) * sc.C + rank;
-    }
+    __device__ static int tile_of(const Params& p, int unit) { return unit / p.S; }
     __device__ static int items(const Params& p, const Sched&, int unit) {
         const int s = unit % p.S;
         const int nb = s * p.nps;
@@ -154,24 +144,18 @@ struct FwdT {
         return max(ne - nb, 0);
     }
     __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
-    __device__ static Coord coord(const Params& p, const Sched& sc, int unit, int item, int rank) {
+    __device__ static Coord coord(const Params& p, const Sched&, int unit, int item) {
         Coord c;
-        const int tile = tile_of(p, sc, unit, rank);
-        c.t0 = tile < sc.n_tiles ? p.tiles[tile].x : static_cast<int>(p.N);   // phantom: rows past the end
+        c.t0 = p.tiles[tile_of(p, unit)].x;
         c.n0 = ((unit % p.S) * p.nps + item) * kBN;
         return c;
     }
     __device__ static uint32_t tx_bytes(const Params&, const Sched&, const Coord&) { return kStageBytes; }
-    __device__ static void load(const Params&, const Sched& sc, const Coord& c, int k, uint8_t* st, uint64_t* bar,
-                                const CUtensorMap* mA, const CUtensorMap* mA2, const CUtensorMap* mB, int rank) {
+    __device__ static void load(const Params&, const Sched&, const Coord& c, int k, uint8_t* st, uint64_t* bar,
+                                const CUtensorMap* mA, const CUtensorMap* mA2, const CUtensorMap* mB) {
         tma_load_2d(mA, bar, st, k * kBK, c.t0);
         tma_load_2d(mA2, bar, st + 16384, k * kBK, c.t0);
-        const int rows = kBN / sc.C;   // B box height
-        if (sc.C == 1)
-            tma_load_2d(mB, bar, st + 32768, k * kBK, c.n0);
-        else
-            tma_load_2d_mc(mB, bar, st + 32768 + rank * rows * 128, k * kBK, c.n0 + rank * rows,
-                           static_cast<uint16_t>((1u << sc.C) - 1u));
+        tma_load_2d(mB, bar, st + 32768, k * kBK, c.n0);
     }
     template <bool kBf16>
     __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
@@ -184,15 +168,11 @@ struct FwdT {
             umma_f16(acc + 256, desc_kmajor(st + 16384 + kk * 32), b, idesc, accum);
         }
     }
-    __device__ static void epi_begin(const Params& p, const Sched& sc, int unit, int rank, int row, Epi& e) {
-        const int tile = tile_of(p, sc, unit, rank);
-        e.valid = false;
-        e.t = 0;
-        if (tile < sc.n_tiles) {
-            const int2 tl = p.tiles[tile];
-            e.t = tl.x + row;
-            e.valid = row < tl.y && GRPO_DCHECK(e.t >= 0 && e.t < p.N, p.status);
-        }
+    __device__ static void epi_begin(const Params& p, const Sched&, int unit, int row, Epi& e) {
+        const int2 tl = p.tiles[tile_of(p, unit)];
+        e.t = tl.x + row;
+        e.valid = row < tl.y && GRPO_DCHECK(e.t >= 0 && e.t < p.N, p.status);
+        if (!e.valid) e.t = 0;
         e.tok = e.valid ? p.tokens[e.t] : -1;
         e.split = unit % p.S;
         e.m[0] = e.m[1] = -INFINITY;
@@ -201,8 +181,7 @@ struct FwdT {
         e.found = false;
     }
     template <bool kBf16>
-    __device__ static void epi_item(const Params& p, const Sched&, int unit, int item, int, uint32_t tacc,
-                                    Epi& e) {
+    __device__ static void epi_item(const Params& p, const Sched&, int unit, int item, uint32_t tacc, Epi& e) {
         const int n0 = ((unit % p.S) * p.nps + item) * kBN;
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
@@ -267,20 +246,15 @@ __device__ __forceinline__ bool chunk_setup(const ChunkParams& p, ChunkSched& sc
 
 // ====================================================================== engine
 
-template <class T, bool kBf16, int kC>
+template <class T, bool kBf16>
 __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUtensorMap& mA, const CUtensorMap& mA2,
                                         const CUtensorMap& mB) {
     extern __shared__ uint8_t smem_raw[];
     typename T::Sched sc;
-    // uniform across the cluster: every CTA reads the same counters
-    if (!T::setup(p, sc, kC)) return;
-    const int cid = static_cast<int>(blockIdx.x) / kC;
-    const int n_clusters = static_cast<int>(gridDim.x) / kC;
-    if (cid >= sc.n_units) return;   // no work for this cluster: leave before touching TMEM
-    const int rank = kC > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    constexpr uint16_t kMask = static_cast<uint16_t>((1u << kC) - 1u);
-    // single CTAs take units from a per-launch counter; clusters walk a fixed stride
-    int* const sched = kC == 1 ? p.sched : nullptr;
+    if (!T::setup(p, sc)) return;
+    if (static_cast<int>(blockIdx.x) >= sc.n_units) return;   // no work for this CTA: leave before touching TMEM
+    // CTAs take work units from a per-launch counter
+    int* const sched = p.sched;
 
     Smem sm = carve_smem<T::kStages, T::kStageBytes>(smem_raw);
     const int warp = threadIdx.x >> 5;
@@ -290,7 +264,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::kStages; ++s) {
             mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kC);   // released by the MMA warp of every CTA in the cluster
+            mbar_init(&sm.empty[s], 1);    // released by the MMA commit
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.acc_full[b], 1);
@@ -315,8 +289,6 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     }
     tc_fence_before();
     __syncthreads();
-    // no CTA may multicast into a peer before the peer's barriers exist
-    if (kC > 1) cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *sm.tmem_slot;
 
@@ -325,15 +297,8 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
         if (lane == 0) {
             int s = 0, us = 0;
             uint32_t ph = 0, uph = 0;
-            int next = cid;
             while (true) {
-                int unit;
-                if (sched) {
-                    unit = atomicAdd(sched, 1);
-                } else {
-                    unit = next;
-                    next += n_clusters;
-                }
+                const int unit = atomicAdd(sched, 1);
                 // publish the unit to the MMA and epilogue roles
                 if (!mbar_wait(&sm.unit_empty[us], uph ^ 1u, sm.abort_flag, status)) goto producer_done;
                 sm.unit_id[us] = unit;
@@ -346,15 +311,13 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
                 const int n_items = T::items(p, sc, unit);
                 const int ks = T::ksteps(p, sc, unit);
                 for (int item = 0; item < n_items; ++item) {
-                    const typename T::Coord c = T::coord(p, sc, unit, item, rank);
+                    const typename T::Coord c = T::coord(p, sc, unit, item);
                     const uint32_t bytes = T::tx_bytes(p, sc, c);
                     for (int k = 0; k < ks; ++k) {
-                        // the stage must be free in every CTA this one multicasts into
                         if (!mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, status)) goto producer_done;
                         uint8_t* st = sm.stages + s * T::kStageBytes;
-                        // bytes landing here: own A and every CTA's slice of B
                         mbar_arrive_expect_tx(&sm.full[s], bytes);
-                        T::load(p, sc, c, k, st, &sm.full[s], &mA, &mA2, &mB, rank);
+                        T::load(p, sc, c, k, st, &sm.full[s], &mA, &mA2, &mB);
                         if (++s == T::kStages) {
                             s = 0;
                             ph ^= 1u;
@@ -391,10 +354,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
                         if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, status)) goto mma_done;
                         tc_fence_after();
                         T::template mma<kBf16>(smem_u32(sm.stages + s * T::kStageBytes), acc, k == 0);
-                        if (kC > 1)
-                            umma_commit_mc(&sm.empty[s], kMask);
-                        else
-                            umma_commit(&sm.empty[s]);
+                        umma_commit(&sm.empty[s]);
                         if (++s == T::kStages) {
                             s = 0;
                             ph ^= 1u;
@@ -405,7 +365,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
             }
         mma_done:
             // every issued MMA (and every commit it feeds) must have finished
-            // before TMEM is released or a peer CTA exits
+            // before TMEM is released
             umma_commit(sm.drain);
             {
                 const uint32_t a = smem_u32(sm.drain);
@@ -436,13 +396,13 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
             if (unit >= sc.n_units) break;
             const int n_items = T::items(p, sc, unit);
             typename T::Epi e;
-            T::epi_begin(p, sc, unit, rank, row, e);
+            T::epi_begin(p, sc, unit, row, e);
             for (int item = 0; item < n_items; ++item, ++it) {
                 const int b = T::kAccBufs == 1 ? 0 : (it & 1);
                 const uint32_t aph = static_cast<uint32_t>(T::kAccBufs == 1 ? it : (it >> 1)) & 1u;
                 if (!mbar_wait(&sm.acc_full[b], aph, sm.abort_flag, status)) goto epi_done;
                 tc_fence_after();
-                T::template epi_item<kBf16>(p, sc, unit, item, rank, tq + b * T::kAccStride, e);
+                T::template epi_item<kBf16>(p, sc, unit, item, tq + b * T::kAccStride, e);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.acc_empty[b]);
@@ -456,8 +416,6 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     tc_fence_before();
     __syncthreads();
     abort_grace(sm.abort_flag);
-    // peers may still multicast into this CTA's shared memory until they are done
-    if (kC > 1) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -473,8 +431,8 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
 // Work-unit orders.  A unit is a pair (a, b); the a-indices are visited in
 // groups of G: all b of a group run before the next group starts, and within a
 // group the a-indices are fastest.  With G = 1 the b-index is fastest.  The
-// group sizes were chosen by timing on GB300 (16 row tiles per group for the
-// chunk forward: each W tile is then shared in L2 by 16 tiles).
+// group sizes were chosen by timing on GB300 (19 row tiles per group for the
+// chunk forward: each W tile is then shared in L2 by 19 tiles).
 constexpr int kFwdGroup = 19;   // chunk forward: a = 128-row tile, b = vocabulary split (19 divides 38 and 76)
 constexpr int kDhGroup = 1;     // dH: a = pair of 128-row tiles, b = 256-wide d tile
 constexpr int kDwGroup = 1;     // dW: a = pair of 128-row vocabulary tiles, b = 256-wide d tile
@@ -1057,11 +1015,11 @@ cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cud
 
 // One named kernel per traits class (the names show up in profiles).
 #define GRPO_TC_KERNEL(NAME, TRAITS)                                                                           \
-    template <bool kBf16, int kC>                                                                              \
+    template <bool kBf16>                                                                                      \
     __global__ void __launch_bounds__(kThreads, 1)                                                             \
         NAME(const __grid_constant__ TRAITS::Params p, const __grid_constant__ CUtensorMap mA,                 \
              const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB) {                \
-        tc_body<TRAITS, kBf16, kC>(p, mA, mA2, mB);                                                            \
+        tc_body<TRAITS, kBf16>(p, mA, mA2, mB);                                                                \
     }
 
 GRPO_TC_KERNEL(grpo_fwd_lse_kernel, FwdT)
@@ -1139,8 +1097,8 @@ cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr, const CUtensorMap& mW,
                        int n_sm, bool bf16, cudaStream_t st) {
-    return bf16 ? launch_tc<FwdT, kClusterFwd>(grpo_fwd_lse_kernel<true, kClusterFwd>, p, mHp, mHr, mW, n_sm, st)
-                : launch_tc<FwdT, kClusterFwd>(grpo_fwd_lse_kernel<false, kClusterFwd>, p, mHp, mHr, mW, n_sm, st);
+    return bf16 ? launch_tc<FwdT, 1>(grpo_fwd_lse_kernel<true>, p, mHp, mHr, mW, n_sm, st)
+                : launch_tc<FwdT, 1>(grpo_fwd_lse_kernel<false>, p, mHp, mHr, mW, n_sm, st);
 }
 
 }  // namespace grpo
