@@ -187,6 +187,48 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
                       void* dH, float* dW, int32_t* found_inf, float* row_stats,
                       int32_t* status, grpo_stream_t stream);
 
+/* ---- data-parallel shards ---------------------------------------------
+ * A batch of prompt groups split over several GPUs, each holding W and whole
+ * prompt groups (so advantages need no exchange).  The loss is still the
+ * mean over the completion tokens of the WHOLE batch ("Long-context GRPO",
+ * section 4: the objective averaged over completion tokens); the pages
+ * describe one GPU, so the split itself is this library's.  Protocol:
+ *   1. each shard: grpo_shard_counts(mask) -> its two counts (device);
+ *   2. the caller sums the counts over the shards (e.g. an all-reduce);
+ *   3. each shard: grpo_loss_fwd_bwd_shard(..., global_counts, ...);
+ *   4. the caller sums loss_out and dW over the shards.
+ * Every shard's weights use the global counts, so the summed loss and dW equal
+ * a one-GPU call on the whole batch up to rounding, and each shard's dH rows
+ * are exactly the whole batch's dH rows.
+ *
+ * grpo_shard_counts: counts_out [2] int32 (device, written) <- (masked-in
+ * rows, completions with at least one masked-in row) of this shard's mask
+ * [n_groups*G*L] uint8 (device).  Asynchronous on `stream`. */
+int grpo_shard_counts(const uint8_t* mask, const grpo_shape* shape, int32_t* counts_out, grpo_stream_t stream);
+
+/* One shard's forward (+ backward): the arguments of grpo_loss_fwd /
+ * grpo_loss_fwd_bwd for this shard's rows (shape describes the shard:
+ * n_groups is its own group count), plus
+ *   global_counts [2] int32 (device, read): the sums over all shards of
+ *     grpo_shard_counts, i.e. (N_v of the batch, active completions of the batch)
+ * and with these meanings of the outputs:
+ *   loss_out: this shard's share of the batch loss, i.e. the sum of its rows'
+ *     weighted objectives divided by the batch's divisor; the shares add up
+ *     to the batch loss
+ *   dW: this shard's share of the batch gradient (sum over shards = dW)
+ *   dH: the batch gradient of this shard's rows (no sum needed)
+ * Global counts below this shard's own counts set *status to GRPO_ERR_SHAPE.
+ * Workspace, alignment and every other rule are those of grpo_loss_fwd_bwd. */
+int grpo_loss_fwd_shard(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                        const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                        const int32_t* global_counts, void* workspace, size_t ws_bytes, float* loss_out,
+                        float* row_stats, int32_t* status, grpo_stream_t stream);
+int grpo_loss_fwd_bwd_shard(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                            const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                            const int32_t* global_counts, float loss_scale, void* workspace, size_t ws_bytes,
+                            float* loss_out, void* dH, float* dW, int32_t* found_inf, float* row_stats,
+                            int32_t* status, grpo_stream_t stream);
+
 /* Forward pass on 8-bit inputs ("Long-context GRPO", section 3: linear cross
  * entropy under float8 mixed precision).  h_pol, h_ref and W hold OCP FP8
  * codes of one format, shape->dtype: GRPO_E4M3 (4 exponent bits, 3 mantissa
@@ -219,8 +261,11 @@ int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float
  *   Limit: N = n_groups*G*L <= 32768 rows; larger shapes are rejected with
  *   GRPO_ERR_WORKSPACE before anything is launched.
  *   The first call on a device looks up the array's device address (a
- *   synchronous runtime call); make that first call before any stream
- *   capture.
+ *   synchronous runtime call).  Under lazy module loading (the CUDA default)
+ *   that first call is also when the driver loads this library's device code
+ *   and places the array in device memory, so make it before the device's
+ *   free memory is handed to anything else (an inference engine's pool), and
+ *   before any stream capture; later calls need no new memory.
  *   Every call uses the same array, so calls that can overlap on the GPU
  *   (other streams, other host threads) race; serialise them.  Nothing
  *   carries over between calls: each call writes every word it reads. */

@@ -62,6 +62,10 @@ def _L():
         lib.oracle_logsumexp.argtypes = [p, i32]
         lib.oracle_row_terms.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, f64, i32, p, i64, p]
         lib.oracle_row_weights.argtypes = [p, i64, i32, i32, p]
+        lib.oracle_shard_counts.argtypes = [p, i32, i32, p]
+        lib.oracle_row_weights_shard.argtypes = [p, i64, i32, i32, i64, i64, p]
+        lib.oracle_weighted_sum.restype = f64
+        lib.oracle_weighted_sum.argtypes = [p, p, i64]
         lib.oracle_reduce_loss.restype = f64
         lib.oracle_reduce_loss.argtypes = [p, p, i64, i32, i32]
         lib.oracle_loss.restype = f64
@@ -173,6 +177,31 @@ def row_weights(rows, L, loss_mode=0):
     out = np.empty(rows.size, np.float64)
     _L().oracle_row_weights(_p(rows), rows.size, L, _mode(loss_mode), _p(out))
     return out
+
+
+def shard_counts(mask, n_seq, L):
+    """(masked-in rows, completions with a masked-in row) of one shard's mask."""
+    m = np.ascontiguousarray(mask, np.uint8)
+    out = np.zeros(2, np.int64)
+    _L().oracle_shard_counts(_p(m), int(n_seq), int(L), _p(out))
+    return int(out[0]), int(out[1])
+
+
+def row_weights_shard(rows, L, n_valid_batch, n_active_batch, loss_mode=0):
+    """Loss weights of one shard's masked-in rows when the batch's divisors
+    (all shards' masked-in rows and active completions) are given."""
+    rows = np.ascontiguousarray(rows, np.int32)
+    out = np.empty(rows.size, np.float64)
+    _L().oracle_row_weights_shard(_p(rows), rows.size, L, _mode(loss_mode), int(n_valid_batch),
+                                  int(n_active_batch), _p(out))
+    return out
+
+
+def weighted_sum(ell, w):
+    """sum_i w_i ell_i (a shard's share of the batch loss)."""
+    ell = np.ascontiguousarray(ell, np.float64)
+    w = np.ascontiguousarray(w, np.float64)
+    return float(_L().oracle_weighted_sum(_p(ell), _p(w), ell.size))
 
 
 def reduce_loss(ell, rows, L, loss_mode=0):

@@ -160,6 +160,19 @@ int64_t oracle_valid_rows(const uint8_t* mask, int64_t N, int32_t* rows) {
     return n;
 }
 
+/* counts of one shard of a batch: out[0] = masked-in rows, out[1] =
+ * completions with at least one masked-in row */
+void oracle_shard_counts(const uint8_t* mask, int n_seq, int L, int64_t* out) {
+    out[0] = 0;
+    out[1] = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        int64_t c = 0;
+        for (int j = 0; j < L; ++j) c += mask[(size_t)i * L + j] != 0;
+        out[0] += c;
+        out[1] += c > 0;
+    }
+}
+
 /* ---- logits of one row and their logsumexp ------------------------------ */
 
 /* widen row r of a [*, d] matrix into out[d] */
@@ -301,6 +314,34 @@ void oracle_row_weights(const int32_t* rows, int64_t n_rows, int L, int loss_mod
     } else {
         for (int64_t i = 0; i < n_rows; ++i) w[i] = 1.0 / (double)n_rows;
     }
+}
+
+/* The same weights for one shard of a batch split by whole completions over
+ * several devices: the divisors count the whole batch, so that the shards'
+ * weighted sums add up to the batch's mean.
+ *   loss_mode 0: 1 / n_valid_batch
+ *   loss_mode 1: 1 / (n_active_batch * len_i), len_i counted in this shard's
+ *                rows (a completion lies wholly in one shard) */
+void oracle_row_weights_shard(const int32_t* rows, int64_t n_rows, int L, int loss_mode, int64_t n_valid_batch,
+                              int64_t n_active_batch, double* w) {
+    if (loss_mode == 1) {
+        int64_t i = 0;
+        while (i < n_rows) {
+            int64_t seq = rows[i] / L, j = i;
+            while (j < n_rows && rows[j] / L == seq) ++j;
+            for (int64_t k = i; k < j; ++k) w[k] = 1.0 / ((double)n_active_batch * (double)(j - i));
+            i = j;
+        }
+    } else {
+        for (int64_t i = 0; i < n_rows; ++i) w[i] = 1.0 / (double)n_valid_batch;
+    }
+}
+
+/* sum_i w_i * ell_i in ascending order: one shard's share of the batch loss */
+double oracle_weighted_sum(const double* ell, const double* w, int64_t n) {
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s = s + w[i] * ell[i];
+    return s;
 }
 
 /* The loss from per-row objectives of all masked-in rows (ascending):

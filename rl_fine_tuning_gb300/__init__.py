@@ -18,6 +18,7 @@ __all__ = [
     "GrpoError", "GrpoShape", "BF16", "FP16", "E4M3", "E5M2", "TOKEN_MEAN", "SEQUENCE_MEAN", "OBJECTIVES", "load",
     "make_shape", "grpo_workspace_bytes", "grpo_chunk_rows", "grpo_group_advantages", "grpo_build_mask",
     "grpo_valid_rows", "grpo_loss_fwd", "grpo_loss_fwd_bwd", "grpo_loss_fwd_fp8", "grpo_loss_fwd_noalloc",
+    "grpo_shard_counts", "grpo_loss_fwd_shard", "grpo_loss_fwd_bwd_shard",
     "grpo_status_string", "grpo_version", "library_path", "grpo_profile_enable", "grpo_profile_collect",
     "grpo_kernel_launches", "grpo_device_checks", "grpo_selftest_bounds_check", "grpo_selftest_wait_timeout",
     "PROF_KINDS",
@@ -89,6 +90,9 @@ def _declare(lib):
         "grpo_loss_fwd_bwd": ([p, p, p, p, p, p, sp, f32, p, sz, p, p, p, p, p, p, p], i32),
         "grpo_loss_fwd_fp8": ([p, p, p, f32, f32, f32, p, p, p, sp, p, sz, p, p, p, p], i32),
         "grpo_loss_fwd_noalloc": ([p, p, p, p, p, p, sp, p, p, p, p], i32),
+        "grpo_shard_counts": ([p, sp, p, p], i32),
+        "grpo_loss_fwd_shard": ([p, p, p, p, p, p, sp, p, p, sz, p, p, p, p], i32),
+        "grpo_loss_fwd_bwd_shard": ([p, p, p, p, p, p, sp, p, f32, p, sz, p, p, p, p, p, p, p], i32),
         "grpo_profile_enable": ([i32], i32),
         "grpo_profile_collect": ([ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_longlong), i32], i32),
         "grpo_kernel_launches": ([], ctypes.c_ulonglong),
@@ -183,6 +187,28 @@ def grpo_loss_fwd_bwd(h_pol, h_ref, W, tokens, mask, adv, shape, loss_scale, wor
                                     ctypes.byref(shape), float(loss_scale), _ptr(workspace), _nbytes(workspace),
                                     _ptr(loss_out), _ptr(dH), _ptr(dW), _ptr(found_inf), _ptr(row_stats),
                                     _ptr(status), _stream(stream)), "grpo_loss_fwd_bwd")
+
+
+def grpo_shard_counts(mask, shape, counts_out, stream=None):
+    _check(load().grpo_shard_counts(_ptr(mask), ctypes.byref(shape), _ptr(counts_out), _stream(stream)),
+           "grpo_shard_counts")
+
+
+def grpo_loss_fwd_shard(h_pol, h_ref, W, tokens, mask, adv, shape, global_counts, workspace, loss_out, row_stats,
+                        status, stream=None):
+    _check(load().grpo_loss_fwd_shard(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv),
+                                      ctypes.byref(shape), _ptr(global_counts), _ptr(workspace), _nbytes(workspace),
+                                      _ptr(loss_out), _ptr(row_stats), _ptr(status), _stream(stream)),
+           "grpo_loss_fwd_shard")
+
+
+def grpo_loss_fwd_bwd_shard(h_pol, h_ref, W, tokens, mask, adv, shape, global_counts, loss_scale, workspace,
+                            loss_out, dH, dW, found_inf, row_stats, status, stream=None):
+    _check(load().grpo_loss_fwd_bwd_shard(_ptr(h_pol), _ptr(h_ref), _ptr(W), _ptr(tokens), _ptr(mask), _ptr(adv),
+                                          ctypes.byref(shape), _ptr(global_counts), float(loss_scale),
+                                          _ptr(workspace), _nbytes(workspace), _ptr(loss_out), _ptr(dH), _ptr(dW),
+                                          _ptr(found_inf), _ptr(row_stats), _ptr(status), _stream(stream)),
+           "grpo_loss_fwd_bwd_shard")
 
 
 def grpo_status_string(code: int) -> str:

@@ -257,6 +257,7 @@ struct Inputs {
     float* loss_out;
     float* row_stats;
     int32_t* status;
+    const int32_t* global_counts = nullptr;   // a data-parallel shard: every shard's counts (device [2])
 };
 
 int validate(const Inputs& in, WsLayout* L) {
@@ -332,6 +333,12 @@ int run_index(const Inputs& in, const WsLayout& L, char* w, cudaStream_t st) {
         launch(GRPO_PROF_INDEX, st, [&] {
             return launch_seq_counts(in.mask, L.n_seq, in.shape->L, reinterpret_cast<int*>(w + L.seqcnt),
                                      reinterpret_cast<int*>(w + L.counts), st);
+        }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    if (in.global_counts &&
+        launch(GRPO_PROF_INDEX, st, [&] {
+            return launch_apply_global_counts(in.global_counts, reinterpret_cast<int*>(w + L.counts),
+                                              in.shape->loss_mode, in.status, st);
         }) != cudaSuccess)
         return GRPO_ERR_LAUNCH;
     return GRPO_OK;
@@ -606,6 +613,54 @@ int grpo_loss_fwd_bwd(const void* h_pol, const void* h_ref, const void* W, const
     WsLayout L;
     int rc = validate(in, &L);
     if (rc != GRPO_OK) return rc;
+    if (!dH || !dW || !found_inf || !aligned(dH, 32) || !aligned(dW, 32) || !aligned(found_inf, 4))
+        return GRPO_ERR_POINTER;
+    if (!(loss_scale > 0.f) || !std::isfinite(loss_scale)) return GRPO_ERR_SHAPE;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    const Backward bwd{loss_scale, dH, dW, found_inf};
+    return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), &bwd);
+}
+
+int grpo_shard_counts(const uint8_t* mask, const grpo_shape* shape, int32_t* counts_out, grpo_stream_t stream) {
+    if (!shape || !shape_ok(*shape)) return GRPO_ERR_SHAPE;
+    if (!mask || !counts_out || !aligned(counts_out, 4)) return GRPO_ERR_POINTER;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return launch(GRPO_PROF_INDEX, st, [&] {
+               return launch_shard_counts(mask, shape->n_groups * shape->G, shape->L, counts_out, st);
+           }) == cudaSuccess
+               ? GRPO_OK
+               : GRPO_ERR_LAUNCH;
+}
+
+int grpo_loss_fwd_shard(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                        const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                        const int32_t* global_counts, void* workspace, size_t ws_bytes, float* loss_out,
+                        float* row_stats, int32_t* status, grpo_stream_t stream) {
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, workspace, ws_bytes, loss_out, row_stats, status};
+    in.global_counts = global_counts;
+    WsLayout L;
+    int rc = validate(in, &L);
+    if (rc != GRPO_OK) return rc;
+    if (!global_counts || !aligned(global_counts, 4)) return GRPO_ERR_POINTER;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+int grpo_loss_fwd_bwd_shard(const void* h_pol, const void* h_ref, const void* W, const int32_t* tokens,
+                            const uint8_t* mask, const float* adv, const grpo_shape* shape,
+                            const int32_t* global_counts, float loss_scale, void* workspace, size_t ws_bytes,
+                            float* loss_out, void* dH, float* dW, int32_t* found_inf, float* row_stats,
+                            int32_t* status, grpo_stream_t stream) {
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, workspace, ws_bytes, loss_out, row_stats, status};
+    in.global_counts = global_counts;
+    WsLayout L;
+    int rc = validate(in, &L);
+    if (rc != GRPO_OK) return rc;
+    if (!global_counts || !aligned(global_counts, 4)) return GRPO_ERR_POINTER;
     if (!dH || !dW || !found_inf || !aligned(dH, 32) || !aligned(dW, 32) || !aligned(found_inf, 4))
         return GRPO_ERR_POINTER;
     if (!(loss_scale > 0.f) || !std::isfinite(loss_scale)) return GRPO_ERR_SHAPE;

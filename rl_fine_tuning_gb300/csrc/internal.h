@@ -50,10 +50,21 @@ enum CountSlot {
     C_NTILES = 1,      // forward row tiles
     C_NCHUNKS = 2,     // backward chunks
     C_CHUNK_ROWS = 3,  // rows per backward chunk (multiple of 128)
-    C_WINV = 4,        // 1 / max(N_valid, 1) as float bits
+    C_WINV = 4,        // 1 / max(N_div, 1) as float bits: the weight of one row in the token mean
     C_NACT = 5,        // completions with at least one masked-in row
+    C_SHARD = 6,       // 1 when the divisors below come from the caller's global counts (a data-parallel shard)
+    C_NDIV_G = 7,      // shard: masked-in rows over all shards (the token mean's divisor)
+    C_NACT_G = 8,      // shard: completions with a masked-in row over all shards (the sequence mean's divisor)
     C_COUNT_WORDS = 16
 };
+
+// divisors of the mean: this call's own counts, or the global ones of a shard
+__device__ __forceinline__ int count_ndiv(const int* counts) {
+    return counts[C_SHARD] ? counts[C_NDIV_G] : counts[C_NVALID];
+}
+__device__ __forceinline__ int count_nact(const int* counts) {
+    return counts[C_SHARD] ? counts[C_NACT_G] : counts[C_NACT];
+}
 
 struct WsLayout {
     size_t counts, sched, seqcnt, tiles, rows, part, zt, lse, gco, ell, blocksum, hc, hcr, partc, mx, ds, total;
@@ -145,6 +156,11 @@ cudaError_t launch_advantages(const float* r, int n_groups, int G, float eps, in
 cudaError_t launch_build_mask(const int32_t* lengths, int n_seq, int L, uint8_t* mask, cudaStream_t st);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_seq_counts(const uint8_t* mask, int n_seq, int L, int* seqcnt, int* counts, cudaStream_t st);
+// data-parallel shards: this shard's (masked-in rows, active completions), and the
+// switch of the divisors to the caller's global counts
+cudaError_t launch_shard_counts(const uint8_t* mask, int n_seq, int L, int* out, cudaStream_t st);
+cudaError_t launch_apply_global_counts(const int* global_counts, int* counts, int loss_mode, int* status,
+                                       cudaStream_t st);
 cudaError_t launch_rows_init(const uint8_t* mask, int64_t N, float* ell, float* row_stats, int sm_count,
                              cudaStream_t st);
 cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, int nblk, const int* counts,

@@ -198,6 +198,9 @@ __global__ void __launch_bounds__(kIndexThreads) k_index(const uint8_t* __restri
         counts[C_CHUNK_ROWS] = rc;
         counts[C_WINV] = __float_as_int(1.0f / static_cast<float>(nv > 0 ? nv : 1));
         counts[C_NACT] = 0;   // counted by k_seq_counts
+        counts[C_SHARD] = 0;  // set by k_apply_global_counts for a shard
+        counts[C_NDIV_G] = 0;
+        counts[C_NACT_G] = 0;
     }
 }
 
@@ -326,8 +329,9 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
             if (p.loss_mode == GRPO_SEQUENCE_MEAN) {
                 // weight N_v / (n_active * len_i): the final division by N_v
                 // then yields the mean over completions of their token means
-                const int nv = p.counts[C_NVALID];
-                const int nact = p.counts[C_NACT];
+                // (for a shard, N_v and n_active count every shard's rows)
+                const int nv = count_ndiv(p.counts);
+                const int nact = count_nact(p.counts);
                 const int len = p.seqcnt[t / p.L];
                 const float rel = static_cast<float>(static_cast<double>(nv) /
                                                      (static_cast<double>(nact) * static_cast<double>(len)));
@@ -388,6 +392,61 @@ cudaError_t launch_seq_counts(const uint8_t* mask, int n_seq, int L, int* seqcnt
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ data-parallel shards
+// One shard's counts: out[0] = masked-in rows, out[1] = completions with at
+// least one masked-in row (out zeroed beforehand; integer atomics, so the
+// result does not depend on the order the blocks finish in).
+__global__ void k_shard_counts(const uint8_t* __restrict__ mask, int n_seq, int L, int* __restrict__ out) {
+    __shared__ int sh[256];
+    for (int i = blockIdx.x; i < n_seq; i += gridDim.x) {
+        const uint8_t* m = mask + static_cast<int64_t>(i) * L;
+        int c = 0;
+        for (int j = threadIdx.x; j < L; j += 256) c += m[j] != 0;
+        sh[threadIdx.x] = c;
+        __syncthreads();
+        for (int s = 128; s > 0; s >>= 1) {
+            if (threadIdx.x < s) sh[threadIdx.x] += sh[threadIdx.x + s];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0 && sh[0] > 0) {
+            atomicAdd(out, sh[0]);
+            atomicAdd(out + 1, 1);
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_shard_counts(const uint8_t* mask, int n_seq, int L, int* out, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(out, 0, 2 * sizeof(int), st);
+    if (e != cudaSuccess) return e;
+    int blocks = n_seq < 4096 ? n_seq : 4096;
+    if (blocks < 1) blocks = 1;
+    k_shard_counts<<<blocks, 256, 0, st>>>(mask, n_seq, L, out);
+    return cudaGetLastError();
+}
+
+// A shard of a data-parallel batch ("partition by whole prompt groups"): the
+// token mean divides by the masked-in rows of ALL shards, and the sequence
+// mean by all shards' active completions, so the shards' losses and dW add up
+// to those of the whole batch.  Runs after the row index (and the completion
+// counts): global counts smaller than this shard's own are an error.
+__global__ void k_apply_global_counts(const int* __restrict__ g, int* __restrict__ counts, int loss_mode,
+                                      int* status) {
+    const int nv_g = g[0], nact_g = g[1];
+    const bool bad = nv_g < counts[C_NVALID] || (loss_mode == GRPO_SEQUENCE_MEAN && nact_g < counts[C_NACT]);
+    if (bad) atomicCAS(status, 0, GRPO_ERR_SHAPE);
+    counts[C_SHARD] = 1;
+    counts[C_NDIV_G] = nv_g;
+    counts[C_NACT_G] = nact_g;
+    counts[C_WINV] = __float_as_int(1.0f / static_cast<float>(nv_g > 0 ? nv_g : 1));
+}
+
+cudaError_t launch_apply_global_counts(const int* global_counts, int* counts, int loss_mode, int* status,
+                                       cudaStream_t st) {
+    k_apply_global_counts<<<1, 1, 0, st>>>(global_counts, counts, loss_mode, status);
+    return cudaGetLastError();
+}
+
 // masked rows: objective 0 and zero diagnostics (the chunked merge never visits them)
 __global__ void k_rows_init(const uint8_t* __restrict__ mask, int64_t N, float* __restrict__ ell,
                             float* __restrict__ row_stats) {
@@ -437,7 +496,7 @@ __global__ void __launch_bounds__(1024) k_loss_final(const double* __restrict__ 
         __syncthreads();
     }
     if (threadIdx.x == 0) {
-        const int nv = counts[C_NVALID];
+        const int nv = count_ndiv(counts);
         *loss_out = nv > 0 ? static_cast<float>(sh[0] / static_cast<double>(nv)) : 0.f;
     }
 }

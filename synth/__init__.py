@@ -250,3 +250,23 @@ def generate(cfg: Config, seed: int = 0, with_w: bool = True) -> Workload:
     tokens = uniform_int(seed, S_TOK, N, 0, V - 1)
     return Workload(cfg, h_pol, h_ref, W, tokens, lengths_for(cfg, seed), rewards_for(cfg, seed))
 
+
+
+def split_groups(wl: Workload, n_shards: int) -> list:
+    """The workload cut into n_shards consecutive runs of whole prompt groups
+    (the data-parallel split): shard r holds groups [r*g, (r+1)*g) with
+    g = n_groups / n_shards, i.e. their rows, tokens, lengths and rewards;
+    every shard keeps the whole W."""
+    from dataclasses import replace
+    cfg = wl.cfg
+    assert cfg.n_groups % n_shards == 0, "shards hold whole prompt groups"
+    g = cfg.n_groups // n_shards
+    scfg = replace(cfg, n_groups=g)
+    rows, seqs = scfg.N, scfg.n_seq
+    out = []
+    for r in range(n_shards):
+        rs, ss = slice(r * rows, (r + 1) * rows), slice(r * seqs, (r + 1) * seqs)
+        out.append(Workload(scfg, np.ascontiguousarray(wl.h_pol[rs]), np.ascontiguousarray(wl.h_ref[rs]), wl.W,
+                            np.ascontiguousarray(wl.tokens[rs]), np.ascontiguousarray(wl.lengths[ss]),
+                            np.ascontiguousarray(wl.rewards[ss]), dict(wl.extra)))
+    return out
