@@ -94,3 +94,42 @@ def test_noalloc_rejects_shapes_beyond_its_array():
     with pytest.raises(rg.GrpoError) as e:
         rg.grpo_loss_fwd_noalloc(dummy, dummy, dummy, dummy, dummy, dummy, shape, dummy, None, dummy)
     assert e.value.code == 3          # GRPO_ERR_WORKSPACE
+
+
+_LAZY_SCRIPT = r"""
+import os, sys
+sys.path.insert(0, os.environ["GRPO_ROOT"]); sys.path.insert(0, os.path.join(os.environ["GRPO_ROOT"], "tests"))
+import torch
+import rl_fine_tuning_gb300 as rg
+import synth
+from gpu_harness import DeviceWorkload
+cfg = synth.make_config("tiny", G=8, L=512, d=256, V=3000, len_lo=1, len_hi=512)
+dw = DeviceWorkload(synth.generate(cfg, seed=2))
+outs = [(torch.full((1,), float("nan"), device="cuda"), torch.full((cfg.N, 5), float("nan"), device="cuda"),
+         torch.full((1,), -1, dtype=torch.int32, device="cuda")) for _ in range(2)]
+def call(o):
+    rg.grpo_loss_fwd_noalloc(dw.h_pol, dw.h_ref, dw.W, dw.tokens, dw.mask, dw.adv, dw.shape, o[0], o[1], o[2])
+    torch.cuda.synchronize()
+call(outs[0])                                   # first call on the device: the library's set-up
+free, _ = torch.cuda.mem_get_info()
+hold = torch.empty(free - (256 << 20), dtype=torch.uint8, device="cuda")   # the device's memory handed elsewhere
+free_after, _ = torch.cuda.mem_get_info()
+call(outs[1])
+assert int(outs[0][2].item()) == 0 and int(outs[1][2].item()) == 0
+assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+del hold
+print("OK", free_after >> 20)
+"""
+
+
+def test_noalloc_second_call_needs_no_free_memory_under_lazy_loading():
+    # In a fresh process with lazy module loading: after the first call, all but
+    # 256 MiB of the device's free memory is taken by someone else; the next
+    # call must still run and give the same bits.
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, CUDA_MODULE_LOADING="LAZY", GRPO_ROOT=root)
+    r = subprocess.run([sys.executable, "-c", _LAZY_SCRIPT], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "OK" in r.stdout, (r.stdout[-2000:], r.stderr[-4000:])
