@@ -13,8 +13,12 @@ the pages' long-context run.  Inputs (W 1 GB, hidden states 1.3 GB each) are
 larger than L2, so steps need no L2 flush.
 
 Prints one JSON line (rank 0).  With N>1 (torchrun) each rank runs an
-independent replica of the same workload (the loss has no exchange on one
-GPU); value = all ranks' tokens / max-over-ranks time.
+independent replica of the same workload by default; with --split the N
+ranks hold one batch of N prompt groups as data-parallel shards (each rank
+one group, the same synthetic inputs on every rank): every step sums the
+batch's counts before the loss and the loss shares and dW after it over the
+ranks (NCCL), so each rank ends the step with the batch's loss and dW.
+value = all ranks' tokens / max-over-ranks time.
 
 --impl reference times the fp64 CPU oracle on the host cores on a bounded
 sample of rows of the same workload, each step a different sample.
@@ -36,6 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "GRPO loss fwd+bwd tokens/s and % of bf16 tensor peak on 1 GB300; peak extra HBM"
 DEFAULT_CONFIG = "llama-3.1-8b-20k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DATASHEET_BF16_TFLOPS = 2250.0   # GB300 dense bf16 tensor peak (without sparsity)
 
 
 def parse():
@@ -52,22 +57,42 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target length of one oracle sample")
     ap.add_argument("--forward", action="store_true",
                     help="time the forward-only entry points (bf16 and e4m3 inputs) instead of fwd+bwd")
+    ap.add_argument("--split", action="store_true",
+                    help="with N>1: one batch of N prompt groups split over the ranks (data-parallel shards), "
+                         "the batch counts and dW summed over the ranks every step; default: N replicas")
     return ap.parse_args()
 
 
 # --------------------------------------------------------------------------- ranks
 
 class Ranks:
-    def __init__(self, n_gpus):
+    """The ranks of a torchrun launch: a gloo group for barriers and timings and,
+    for the data-parallel split, a second group (NCCL on GPUs) that sums the
+    shards' counts, loss shares and dW."""
+
+    def __init__(self, n_gpus, split=False, device_backend="nccl"):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.dev_group = None
         if self.world > 1:
             import torch.distributed as dist
             os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
             dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
             self.pg = dist
+            if split:
+                if device_backend == "nccl":
+                    import torch
+                    torch.cuda.set_device(self.local)
+                self.dev_group = dist.new_group(backend=device_backend)
+
+    def sum_(self, *tensors):
+        """In-place sum over the ranks (the shards' exchange); nothing on one rank."""
+        if not self.dev_group:
+            return
+        for t in tensors:
+            self.pg.all_reduce(t, group=self.dev_group)
 
     def barrier(self):
         if self.pg:
@@ -302,22 +327,36 @@ def run_ours(args, ranks):
     N, d, V = cfg.N, cfg.d, cfg.V
     adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
     mask = torch.empty(N, dtype=torch.uint8, device="cuda")
-    dH = torch.empty((N, d), dtype=tdt, device="cuda")
-    dW = torch.empty((V, d), dtype=torch.float32, device="cuda")
-    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    split = ranks.dev_group is not None
+
+    def outputs():
+        return {"dH": torch.empty((N, d), dtype=tdt, device="cuda"),
+                "dW": torch.empty((V, d), dtype=torch.float32, device="cuda"),
+                "loss": torch.zeros(1, dtype=torch.float32, device="cuda")}
+
+    out = outputs()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     found_inf = torch.zeros(1, dtype=torch.int32, device="cuda")
-    mem_before_ws = torch.cuda.memory_allocated()
+    counts = torch.zeros(2, dtype=torch.int32, device="cuda")
     ws_bytes = rg.grpo_workspace_bytes(shape)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     scale = [cfg.loss_scale]
 
-    def step(d_in):
+    def step(d_in, o=None):
+        o = out if o is None else o
         rg.grpo_group_advantages(d_in["rewards"], cfg.n_groups, cfg.G, cfg.eps, True, adv)
         rg.grpo_build_mask(d_in["lengths"], shape, mask)
-        rg.grpo_loss_fwd_bwd(d_in["h_pol"], d_in["h_ref"], W, d_in["tokens"], mask, adv, shape, scale[0], ws, loss,
-                             dH, dW, found_inf, None, status)
+        if not split:
+            rg.grpo_loss_fwd_bwd(d_in["h_pol"], d_in["h_ref"], W, d_in["tokens"], mask, adv, shape, scale[0], ws,
+                                 o["loss"], o["dH"], o["dW"], found_inf, None, status)
+            return
+        # one shard of the batch: the batch's counts, then this rank's share, then the sums
+        rg.grpo_shard_counts(mask, shape, counts)
+        ranks.sum_(counts)
+        rg.grpo_loss_fwd_bwd_shard(d_in["h_pol"], d_in["h_ref"], W, d_in["tokens"], mask, adv, shape, counts,
+                                   scale[0], ws, o["loss"], o["dH"], o["dW"], found_inf, None, status)
+        ranks.sum_(o["dW"], o["loss"])
 
     # warm-up (also settles the fp16 loss scale: halve while the scaled gradients overflow)
     for _ in range(max(args.warmup, 1)):
@@ -330,7 +369,7 @@ def run_ours(args, ranks):
     st_code = int(status.item())
     if st_code != 0:
         raise SystemExit(f"device status {st_code}: {rg.grpo_status_string(st_code)}")
-    if not np.isfinite(loss.item()):
+    if not np.isfinite(out["loss"].item()):
         raise SystemExit("non-finite loss")
 
     # ---------------- device-resident timed region
@@ -371,7 +410,7 @@ def run_ours(args, ranks):
 
     # ---------------- the same step captured once into a CUDA graph and replayed
     graph = None
-    if not args.no_graph:
+    if not args.no_graph and not split:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -396,17 +435,19 @@ def run_ours(args, ranks):
                  "ms_per_step": ms_g / args.steps, "what": "one step captured into a CUDA graph, replayed"}
         del g
 
-    # ---------------- end to end: host inputs copied in, loss read back, every step
-    # Two ways, both through the public API with every step's inputs copied from
-    # pinned host memory inside the timed region: serially before each step, and
-    # overlapped the way a training loop prefetches its next batch (step i+1's
-    # inputs copied on a second stream into a second device buffer set while
-    # step i computes).  The overlapped figure is the headline.
+    # ---------------- end to end: host inputs copied in, results read back, every step
+    # Through the public API with every step's inputs copied from pinned host
+    # memory inside the timed region: serially before each step, and overlapped
+    # the way a training loop prefetches its next batch (step i+1's inputs
+    # copied on a second stream into a second device buffer set while step i
+    # computes).  The headline reads back the loss only: the gradients stay on
+    # the device, where the optimizer step of a trainer consumes them.  A third
+    # variant also copies dH and dW of every step back to pinned host memory (on
+    # a third stream, from two alternating output sets, while the next step runs).
     e2e = None
     if not args.no_e2e:
         loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
         h2d = sum(host[k].numel() * host[k].element_size() for k in host)
-        d2h = 4
         dev2 = {k: torch.empty_like(v) for k, v in dev.items()}
 
         def copy_in(d_in):
@@ -418,18 +459,23 @@ def run_ours(args, ranks):
             for _ in range(n):
                 copy_in(dev)
                 step(dev)
-                loss_host.copy_(loss, non_blocking=True)
+                loss_host.copy_(out["loss"], non_blocking=True)
 
         copy_stream = torch.cuda.Stream()
+        back_stream = torch.cuda.Stream()
         bufs = (dev, dev2)
         copied = [torch.cuda.Event() for _ in bufs]
         consumed = [torch.cuda.Event() for _ in bufs]
+        outs = [out]
+        grads_host = None
 
-        def run_overlapped(n):
+        def run_overlapped(n, grads_back=False):
             copy_stream.wait_stream(stream)
             with torch.cuda.stream(copy_stream):
                 copy_in(bufs[0])
                 copied[0].record(copy_stream)
+            computed = [torch.cuda.Event() for _ in outs]
+            drained = [None for _ in outs]
             for i in range(n):
                 b = i % 2
                 if i + 1 < n:
@@ -440,9 +486,25 @@ def run_ours(args, ranks):
                         copy_in(bufs[nb])
                         copied[nb].record(copy_stream)
                 stream.wait_event(copied[b])
-                step(bufs[b])
+                if not grads_back:
+                    step(bufs[b])
+                    consumed[b].record(stream)
+                    loss_host.copy_(out["loss"], non_blocking=True)
+                    continue
+                ob = i % 2
+                if drained[ob] is not None:
+                    stream.wait_event(drained[ob])              # step i-2's gradients have left this set
+                step(bufs[b], outs[ob])
                 consumed[b].record(stream)
-                loss_host.copy_(loss, non_blocking=True)
+                computed[ob].record(stream)
+                back_stream.wait_event(computed[ob])
+                with torch.cuda.stream(back_stream):
+                    for k in ("dH", "dW", "loss"):
+                        grads_host[k].copy_(outs[ob][k].view(grads_host[k].dtype), non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(back_stream)
+                    drained[ob] = ev
+            stream.wait_stream(back_stream)
 
         def timed(fn):
             fn(1)
@@ -458,12 +520,27 @@ def run_ours(args, ranks):
 
         ms_ser = timed(run_serial)
         ms_ovl = timed(run_overlapped)
-        del dev2
+        # the same loop with the gradients read back every step
+        outs.append(outputs())
+        grads_host = {"dH": torch.empty((N, d), dtype=torch.int16).pin_memory(),
+                      "dW": torch.empty((V, d), dtype=torch.float32).pin_memory(),
+                      "loss": torch.empty(1, dtype=torch.float32).pin_memory()}
+        d2h_grads = sum(t.numel() * t.element_size() for t in grads_host.values())
+        ms_grads = timed(lambda n: run_overlapped(n, grads_back=True))
+        del dev2, grads_host
+        outs.pop()
         e2e = {"value": ranks.world * n_valid * args.steps / (ms_ovl / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": d2h, "ms_per_step": ms_ovl / args.steps,
-               "copies": "step i+1's inputs copied on a second stream during step i (two device input sets)",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": 4, "ms_per_step": ms_ovl / args.steps,
+               "copies": "step i+1's inputs copied on a second stream during step i (two device input sets); "
+                         "the loss read back every step; dH and dW stay on the device for the optimizer",
                "serial": {"value": ranks.world * n_valid * args.steps / (ms_ser / 1e3),
                           "ms_per_step": ms_ser / args.steps, "copies": "before each step, same stream"},
+               "with_gradients": {"value": ranks.world * n_valid * args.steps / (ms_grads / 1e3),
+                                  "ms_per_step": ms_grads / args.steps, "h2d_bytes_per_step": int(h2d),
+                                  "d2h_bytes_per_step": int(d2h_grads),
+                                  "copies": "as the headline, plus dH, dW and the loss of every step copied to "
+                                            "pinned host memory on a third stream while the next step runs "
+                                            "(two device output sets)"},
                "resident": "lm_head weight W"}
 
     # ---------------- roofline of the dominant kernel
@@ -503,6 +580,12 @@ def run_ours(args, ranks):
     useful = 8.0 * n_valid * V * d
     t_step = ms_step / 1e3
     burst = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    useful_tf = useful / t_step / 1e12
+    # the measured GEMM peaks were taken at their own clock under the power cap;
+    # scaled to this run's median SM clock they compare like with like
+    peak_mhz = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
+    run_mhz = clocks["sm_mhz"] if clocks else None
+    at_clock = (useful_tf / sustained * peak_mhz / run_mhz) if (peak_mhz and run_mhz) else None
 
     cpu = None
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
@@ -514,11 +597,16 @@ def run_ours(args, ranks):
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generator; random-init head)",
         "config": cfg_dict(cfg, {"n_valid": n_valid, "chunk_rows": rg.grpo_chunk_rows(shape),
                                  "loss_scale": scale[0]}),
-        "pct_bf16_peak": {"useful_tflops": useful / t_step / 1e12,
-                          "of_burst": useful / t_step / 1e12 / burst,
-                          "of_sustained": useful / t_step / 1e12 / sustained,
-                          "executed_tflops": useful / t_step / 1e12,
-                          "peaks": pk_kind},
+        "pct_bf16_peak": {"useful_tflops": useful_tf,
+                          "of_datasheet_dense": useful_tf / DATASHEET_BF16_TFLOPS,
+                          "of_burst": useful_tf / burst,
+                          "of_sustained": useful_tf / sustained,
+                          "of_sustained_at_equal_clock": at_clock,
+                          "executed_tflops": useful_tf,
+                          "peaks": f"datasheet dense bf16 {DATASHEET_BF16_TFLOPS:.0f} TFLOP/s; burst and sustained: "
+                                   f"cuBLAS bf16 GEMM, {pk_kind}; at equal clock: sustained x its median SM clock "
+                                   f"({peak_mhz} MHz) / this run's ({run_mhz} MHz)"},
+        "cycles_per_step": (ms_step * run_mhz * 1e3) if run_mhz else None,
         "peak_extra_hbm_gb": max(peak_extra, 0) / 1e9 + ws_bytes / 1e9,
         "workspace_gb": ws_bytes / 1e9,
         "logits_not_materialised_gb": 2 * 2 * N * V / 1e9,
@@ -529,7 +617,9 @@ def run_ours(args, ranks):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "clocks": clocks,
-        "loss": float(loss.item()),
+        "loss": float(out["loss"].item()),
+        "parallelism": ("data-parallel shards: one prompt group per rank, batch counts, loss shares and dW summed "
+                        "over the ranks every step" if split else "replicas"),
     }
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
@@ -620,7 +710,7 @@ def cpu_baseline(cfg, wl, args):
 
 def main():
     args = parse()
-    ranks = Ranks(args.gpus)
+    ranks = Ranks(args.gpus, split=args.split and args.impl == "ours")
     try:
         if args.impl == "reference":
             run_reference(args, ranks)
