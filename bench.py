@@ -627,7 +627,8 @@ def run_ours(args, ranks):
 
 def run_forward_modes(args, ranks):
     """Forward-only throughput: grpo_loss_fwd on bf16 inputs and grpo_loss_fwd_fp8 on
-    the same workload quantised to e4m3 and to e5m2 (one scale per tensor)."""
+    the same workload quantised to e4m3 and to e5m2 (one scale per tensor); and
+    forward+backward on the 8-bit inputs (grpo_loss_fwd_bwd_fp8)."""
     import numpy as np
     import torch
 
@@ -680,6 +681,32 @@ def run_forward_modes(args, ranks):
         flops = 4.0 * n_valid * cfg.V * cfg.d
         out[mode] = {"ms_per_step": ms, "tokens_per_s": n_valid / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
                      "loss": float(loss.item())}
+        if mode != "bf16":
+            # the 8-bit forward+backward on the same inputs (dH bf16, dW fp32)
+            dH = torch.empty((cfg.N, cfg.d), dtype=torch.bfloat16, device="cuda")
+            dW = torch.empty((cfg.V, cfg.d), dtype=torch.float32, device="cuda")
+
+            def step_bwd():
+                rg.grpo_group_advantages(rewards, cfg.n_groups, cfg.G, cfg.eps, True, adv)
+                rg.grpo_build_mask(lengths, shape, mask)
+                rg.grpo_loss_fwd_bwd_fp8(*mats, *wl.extra["scales"], tokens, mask, adv, shape, ws, loss, dH, dW,
+                                         None, status)
+
+            for _ in range(max(args.warmup, 1)):
+                step_bwd()
+            torch.cuda.synchronize()
+            if int(status.item()) != 0:
+                raise SystemExit(f"device status {int(status.item())}")
+            e0.record(stream)
+            for _ in range(args.steps):
+                step_bwd()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / args.steps
+            flops = 8.0 * n_valid * cfg.V * cfg.d
+            out[mode + "_fwd_bwd"] = {"ms_per_step": ms, "tokens_per_s": n_valid / (ms / 1e3),
+                                      "tflops": flops / (ms / 1e3) / 1e12, "loss": float(loss.item())}
+            del dH, dW
         del mats, ws, wl
         torch.cuda.empty_cache()
     pk, pk_kind = peaks()

@@ -237,13 +237,33 @@ int grpo_loss_fwd_bwd_shard(const void* h_pol, const void* h_ref, const void* W,
  * scale_h_ref, scale_w > 0).  The logits come from 8-bit tensor-core products
  * accumulated in fp32 and multiplied by scale_h * scale_w; everything after
  * that is as in grpo_loss_fwd.  d must be a multiple of 128; the workspace is
- * grpo_workspace_bytes(shape).  Forward only: dlogits in e4m3 or
- * e5m2 would carry 6-12% error on the sampled token's entry, far above the
- * gradient tolerance, so the backward stays 16-bit. */
+ * grpo_workspace_bytes(shape) (for an 8-bit shape it includes the buffers of
+ * grpo_loss_fwd_bwd_fp8, which this call leaves unused). */
 int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float scale_h_pol, float scale_h_ref,
                       float scale_w, const int32_t* tokens, const uint8_t* mask, const float* adv,
                       const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out, float* row_stats,
                       int32_t* status, grpo_stream_t stream);
+
+/* Forward and backward on 8-bit inputs ("Long-context GRPO", section 3: a
+ * linear cross entropy under float8 mixed precision with automatic scaling
+ * breaks unless the scaling is handled).  Inputs as grpo_loss_fwd_fp8; the
+ * outputs as grpo_loss_fwd_bwd without loss scaling:
+ *   dH [N x d] bf16 (device, written, 32-byte aligned): d loss / d h_pol,
+ *      exactly 0 on masked rows
+ *   dW [V x d] fp32 (device, overwritten, 32-byte aligned): d loss / d W
+ * (gradients with respect to the decoded values code * scale).  Both backward
+ * GEMMs run on 8-bit codes.  The dlogits g (onehot(tok) - softmax) are split:
+ * the one-hot part, which holds the largest entry of every row, is added
+ * exactly in the GEMM epilogues from the decoded inputs; only the softmax part
+ * g * softmax goes through 8-bit codes of the input format, with one scale per
+ * dlogit row for dH and one per 32 vocabulary rows for dW (scales along the
+ * GEMMs' M dimension, so no K-block scales are needed).  Chunks hold at most
+ * 16384 rows (larger chunk_rows give GRPO_ERR_SHAPE).  The workspace is
+ * grpo_workspace_bytes(shape) for the 8-bit shape. */
+int grpo_loss_fwd_bwd_fp8(const void* h_pol, const void* h_ref, const void* W, float scale_h_pol, float scale_h_ref,
+                          float scale_w, const int32_t* tokens, const uint8_t* mask, const float* adv,
+                          const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out, void* dH,
+                          float* dW, float* row_stats, int32_t* status, grpo_stream_t stream);
 
 /* Forward loss for callers that cannot allocate device memory -- for
  * instance a training step that shares the GPU with an inference engine

@@ -18,7 +18,7 @@ __all__ = [
     "GrpoError", "GrpoShape", "BF16", "FP16", "E4M3", "E5M2", "TOKEN_MEAN", "SEQUENCE_MEAN", "OBJECTIVES", "load",
     "make_shape", "grpo_workspace_bytes", "grpo_chunk_rows", "grpo_group_advantages", "grpo_build_mask",
     "grpo_valid_rows", "grpo_loss_fwd", "grpo_loss_fwd_bwd", "grpo_loss_fwd_fp8", "grpo_loss_fwd_noalloc",
-    "grpo_shard_counts", "grpo_loss_fwd_shard", "grpo_loss_fwd_bwd_shard",
+    "grpo_shard_counts", "grpo_loss_fwd_shard", "grpo_loss_fwd_bwd_shard", "grpo_loss_fwd_bwd_fp8",
     "grpo_status_string", "grpo_version", "library_path", "grpo_profile_enable", "grpo_profile_collect",
     "grpo_kernel_launches", "grpo_device_checks", "grpo_selftest_bounds_check", "grpo_selftest_wait_timeout",
     "PROF_KINDS",
@@ -89,6 +89,7 @@ def _declare(lib):
         "grpo_loss_fwd": ([p, p, p, p, p, p, sp, p, sz, p, p, p, p], i32),
         "grpo_loss_fwd_bwd": ([p, p, p, p, p, p, sp, f32, p, sz, p, p, p, p, p, p, p], i32),
         "grpo_loss_fwd_fp8": ([p, p, p, f32, f32, f32, p, p, p, sp, p, sz, p, p, p, p], i32),
+        "grpo_loss_fwd_bwd_fp8": ([p, p, p, f32, f32, f32, p, p, p, sp, p, sz, p, p, p, p, p, p], i32),
         "grpo_loss_fwd_noalloc": ([p, p, p, p, p, p, sp, p, p, p, p], i32),
         "grpo_shard_counts": ([p, sp, p, p], i32),
         "grpo_loss_fwd_shard": ([p, p, p, p, p, p, sp, p, p, sz, p, p, p, p], i32),
@@ -249,6 +250,14 @@ def grpo_loss_fwd_fp8(h_pol, h_ref, W, scale_h_pol, scale_h_ref, scale_w, tokens
                                     float(scale_w), _ptr(tokens), _ptr(mask), _ptr(adv), ctypes.byref(shape),
                                     _ptr(workspace), _nbytes(workspace), _ptr(loss_out), _ptr(row_stats),
                                     _ptr(status), _stream(stream)), "grpo_loss_fwd_fp8")
+
+
+def grpo_loss_fwd_bwd_fp8(h_pol, h_ref, W, scale_h_pol, scale_h_ref, scale_w, tokens, mask, adv, shape, workspace,
+                          loss_out, dH, dW, row_stats, status, stream=None):
+    _check(load().grpo_loss_fwd_bwd_fp8(_ptr(h_pol), _ptr(h_ref), _ptr(W), float(scale_h_pol), float(scale_h_ref),
+                                        float(scale_w), _ptr(tokens), _ptr(mask), _ptr(adv), ctypes.byref(shape),
+                                        _ptr(workspace), _nbytes(workspace), _ptr(loss_out), _ptr(dH), _ptr(dW),
+                                        _ptr(row_stats), _ptr(status), _stream(stream)), "grpo_loss_fwd_bwd_fp8")
 
 
 def grpo_device_checks() -> bool:

@@ -79,6 +79,7 @@ bool shape_ok(const grpo_shape& s) {
 }
 
 bool dtype_ok(const grpo_shape& s) { return s.dtype == GRPO_BF16 || s.dtype == GRPO_FP16; }
+bool dtype_ok_any(const grpo_shape& s) { return dtype_ok(s) || is_fp8(s.dtype); }
 
 template <class P>
 bool aligned(const P* p, size_t a) {
@@ -236,6 +237,15 @@ bool ws_layout(const grpo_shape& s, WsLayout* o) {
     o->partc = take(static_cast<size_t>(o->R) * o->Sc * 16);
     o->mx = take(static_cast<size_t>(o->R) * o->nc32 * 4);
     o->ds = take(static_cast<size_t>(o->R) * o->V_pad * 2);
+    o->rmax = o->qa = o->qb = o->gmax = o->keys = 0;
+    if (is_fp8(s.dtype)) {
+        // the 8-bit backward's buffers (its forward-only entry point needs none of them)
+        o->rmax = take(static_cast<size_t>(N) * 4);
+        o->qa = take(static_cast<size_t>(o->R) * o->V_pad);
+        o->qb = take(static_cast<size_t>(o->R) * o->V_pad);
+        o->gmax = take(static_cast<size_t>(o->nc32) * 4);
+        o->keys = take(static_cast<size_t>(o->R) * 8);
+    }
     o->total = off;
     return true;
 }
@@ -301,6 +311,7 @@ MergeParams merge_params(const Inputs& in, const WsLayout& L, char* w, int chunk
     mp.ell = reinterpret_cast<float*>(w + L.ell);
     mp.row_stats = in.row_stats;
     mp.status = in.status;
+    mp.rmax = nullptr;
     return mp;
 }
 
@@ -393,7 +404,7 @@ struct Backward {
     int32_t* found_inf;
 };
 
-// 8-bit inputs (forward only): the format and the per-tensor scales
+// 8-bit inputs: the format and the per-tensor scales
 struct Fp8Inputs {
     bool e5m2;
     float h_pol, h_ref, w;
@@ -435,6 +446,13 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         // 8-bit inputs: a K-stage is one 128-byte span of 128 elements
         if (!make_map_u8(&mW_k, in.W, s.d, s.V, s.d, 128, kBN / 2) ||
             !make_map_u8(&mHc_k, hc, s.d, L.R, s.d, 128, kBM) || !make_map_u8(&mHcr_k, hcr, s.d, L.R, s.d, 128, kBM))
+            return GRPO_ERR_LAUNCH;
+        // the 8-bit backward: codes of the dlogits' softmax part K-major for dH, MN-major for dW;
+        // W and the compact h_pol rows MN-major (128 x 128-byte boxes)
+        if (bwd && (!make_map_u8(&mDS_k, w + L.qa, s.V, L.R, L.V_pad, 128, 128) ||
+                    !make_map_u8(&mDS_mn, w + L.qb, s.V, L.R, L.V_pad, 128, 128) ||
+                    !make_map_u8(&mW_mn, in.W, s.d, s.V, s.d, 128, 128) ||
+                    !make_map_u8(&mHc_mn, hc, s.d, L.R, s.d, 128, 128)))
             return GRPO_ERR_LAUNCH;
     } else if (!make_map(&mW_k, in.W, bf16, s.d, s.V, s.d, kBK, kBN / 2) ||
                !make_map(&mW_mn, in.W, bf16, s.d, s.V, s.d, 64, kBK) ||
@@ -481,13 +499,35 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     cp.sched = nullptr;
     cp.found_inf = bwd ? bwd->found_inf : nullptr;
     cp.status = in.status;
+    cp.qa = nullptr;
+    cp.qb = nullptr;
+    cp.rmax = nullptr;
+    cp.gmax = nullptr;
+    cp.keys = nullptr;
+    cp.hq = nullptr;
+    cp.wq = nullptr;
+    cp.scale_h = cp.scale_w = 1.f;
+    cp.e5m2 = 0;
+    if (f8 && bwd) {
+        cp.qa = reinterpret_cast<uint8_t*>(w + L.qa);
+        cp.qb = reinterpret_cast<uint8_t*>(w + L.qb);
+        cp.rmax = reinterpret_cast<const float*>(w + L.rmax);
+        cp.gmax = reinterpret_cast<float*>(w + L.gmax);
+        cp.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
+        cp.hq = reinterpret_cast<const uint8_t*>(hc);
+        cp.wq = static_cast<const uint8_t*>(in.W);
+        cp.scale_h = f8->h_pol;
+        cp.scale_w = f8->w;
+        cp.e5m2 = f8->e5m2 ? 1 : 0;
+    }
     const int64_t max_chunks = (L.N + L.R - 1) / L.R;
     for (int64_t c = 0; c < max_chunks; ++c) {
         const int ci = static_cast<int>(c);
         cp.chunk = ci;
         fp.chunk = ci;
         fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
-        const MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
+        MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
+        if (f8 && bwd) mp.rmax = reinterpret_cast<float*>(w + L.rmax);
         if (launch(GRPO_PROF_GATHER, st, [&] {
                 return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, row_bytes, dev.sm_count, st);
             }) != cudaSuccess)
@@ -499,6 +539,19 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
         if (!bwd) continue;
+        if (f8) {
+            if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_f8_group_max(cp, dev.sm_count, st); }) !=
+                    cudaSuccess ||
+                launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform_f8(cp, dev.sm_count, st); }) !=
+                    cudaSuccess ||
+                launch(GRPO_PROF_DLOGITS, st, [&] { return launch_sort_keys(cp, st); }) != cudaSuccess ||
+                launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair_fp8(cp, mDS_k, mW_mn, dev.sm_count, st); }) !=
+                    cudaSuccess ||
+                launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair_fp8(cp, mDS_mn, mHc_mn, dev.sm_count, st); }) !=
+                    cudaSuccess)
+                return GRPO_ERR_LAUNCH;
+            continue;
+        }
         if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, dev.sm_count, st); }) !=
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
@@ -539,11 +592,9 @@ int grpo_chunk_rows(const grpo_shape* shape) {
 }
 
 size_t grpo_workspace_bytes(const grpo_shape* shape) {
-    if (!shape) return 0;
-    grpo_shape s = *shape;
-    if (s.dtype == GRPO_E4M3 || s.dtype == GRPO_E5M2) s.dtype = GRPO_BF16;   // same layout; 8-bit chunks use half
+    if (!shape || !dtype_ok_any(*shape)) return 0;
     WsLayout L;
-    if (!ws_layout(s, &L)) return 0;
+    if (!ws_layout(*shape, &L)) return 0;
     return L.total;
 }
 
@@ -671,28 +722,66 @@ int grpo_loss_fwd_bwd_shard(const void* h_pol, const void* h_ref, const void* W,
     return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), &bwd);
 }
 
+// Shared argument checks of the two 8-bit entry points; on success *L is the
+// 8-bit workspace layout and *s16 the shape the 16-bit steps run with.
+static int validate_fp8(const Inputs& in8, float scale_h_pol, float scale_h_ref, float scale_w, WsLayout* L,
+                        grpo_shape* s16) {
+    if (!in8.shape) return GRPO_ERR_SHAPE;
+    const grpo_shape& s = *in8.shape;
+    if (!is_fp8(s.dtype)) return GRPO_ERR_DTYPE;
+    if (s.d % 128 != 0) return GRPO_ERR_SHAPE;
+    if (!(scale_h_pol > 0.f) || !(scale_h_ref > 0.f) || !(scale_w > 0.f) || !std::isfinite(scale_h_pol) ||
+        !std::isfinite(scale_h_ref) || !std::isfinite(scale_w))
+        return GRPO_ERR_SHAPE;
+    if (!ws_layout(s, L)) return GRPO_ERR_SHAPE;
+    *s16 = s;
+    s16->dtype = GRPO_BF16;
+    Inputs in = in8;
+    in.shape = s16;
+    WsLayout L16;
+    const int rc = validate(in, &L16);
+    if (rc != GRPO_OK) return rc;
+    if (in.ws_bytes < L->total) return GRPO_ERR_WORKSPACE;
+    return GRPO_OK;
+}
+
 int grpo_loss_fwd_fp8(const void* h_pol, const void* h_ref, const void* W, float scale_h_pol, float scale_h_ref,
                       float scale_w, const int32_t* tokens, const uint8_t* mask, const float* adv,
                       const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out, float* row_stats,
                       int32_t* status, grpo_stream_t stream) {
-    if (!shape) return GRPO_ERR_SHAPE;
-    if (shape->dtype != GRPO_E4M3 && shape->dtype != GRPO_E5M2) return GRPO_ERR_DTYPE;
-    if (shape->d % 128 != 0) return GRPO_ERR_SHAPE;
-    if (!(scale_h_pol > 0.f) || !(scale_h_ref > 0.f) || !(scale_w > 0.f) || !std::isfinite(scale_h_pol) ||
-        !std::isfinite(scale_h_ref) || !std::isfinite(scale_w))
-        return GRPO_ERR_SHAPE;
-    // the workspace layout is the 16-bit one (the 8-bit chunk copies use half of it)
-    grpo_shape s16 = *shape;
-    s16.dtype = GRPO_BF16;
-    Inputs in{h_pol, h_ref, W, tokens, mask, adv, &s16, workspace, ws_bytes, loss_out, row_stats, status};
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, workspace, ws_bytes, loss_out, row_stats, status};
     WsLayout L;
-    int rc = validate(in, &L);
+    grpo_shape s16;
+    int rc = validate_fp8(in, scale_h_pol, scale_h_ref, scale_w, &L, &s16);
     if (rc != GRPO_OK) return rc;
     DeviceInfo dev;
     rc = device_info(&dev);
     if (rc != GRPO_OK) return rc;
+    in.shape = &s16;
     const Fp8Inputs f8{shape->dtype == GRPO_E5M2, scale_h_pol, scale_h_ref, scale_w};
     return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), nullptr, &f8);
+}
+
+int grpo_loss_fwd_bwd_fp8(const void* h_pol, const void* h_ref, const void* W, float scale_h_pol, float scale_h_ref,
+                          float scale_w, const int32_t* tokens, const uint8_t* mask, const float* adv,
+                          const grpo_shape* shape, void* workspace, size_t ws_bytes, float* loss_out, void* dH,
+                          float* dW, float* row_stats, int32_t* status, grpo_stream_t stream) {
+    Inputs in{h_pol, h_ref, W, tokens, mask, adv, shape, workspace, ws_bytes, loss_out, row_stats, status};
+    WsLayout L;
+    grpo_shape s16;
+    int rc = validate_fp8(in, scale_h_pol, scale_h_ref, scale_w, &L, &s16);
+    if (rc != GRPO_OK) return rc;
+    if (L.R > kF8SortMax) return GRPO_ERR_SHAPE;
+    if (!dH || !dW || !aligned(dH, 32) || !aligned(dW, 32)) return GRPO_ERR_POINTER;
+    DeviceInfo dev;
+    rc = device_info(&dev);
+    if (rc != GRPO_OK) return rc;
+    in.shape = &s16;
+    // no loss scaling on this path (dH is bf16): found_inf goes to a spare workspace word
+    int32_t* spare_inf = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.counts) + C_SPARE_INF;
+    const Backward bwd{1.f, dH, dW, spare_inf};
+    const Fp8Inputs f8{shape->dtype == GRPO_E5M2, scale_h_pol, scale_h_ref, scale_w};
+    return run_chunked(in, L, dev, reinterpret_cast<cudaStream_t>(stream), &bwd, &f8);
 }
 
 int grpo_device_checks(void) {

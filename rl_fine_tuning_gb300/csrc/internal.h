@@ -55,6 +55,7 @@ enum CountSlot {
     C_SHARD = 6,       // 1 when the divisors below come from the caller's global counts (a data-parallel shard)
     C_NDIV_G = 7,      // shard: masked-in rows over all shards (the token mean's divisor)
     C_NACT_G = 8,      // shard: completions with a masked-in row over all shards (the sequence mean's divisor)
+    C_SPARE_INF = 9,   // found_inf word of the 8-bit backward, which has no loss scaling
     C_COUNT_WORDS = 16
 };
 
@@ -66,8 +67,16 @@ __device__ __forceinline__ int count_nact(const int* counts) {
     return counts[C_SHARD] ? counts[C_NACT_G] : counts[C_NACT];
 }
 
+// The 8-bit backward sorts each chunk's (token, slot) keys in one block's
+// shared memory: chunks of at most this many rows.
+constexpr int kF8SortMax = 16384;
+
 struct WsLayout {
     size_t counts, sched, seqcnt, tiles, rows, part, zt, lse, gco, ell, blocksum, hc, hcr, partc, mx, ds, total;
+    // 8-bit inputs only (grpo_loss_fwd_bwd_fp8): row maxima [N] f32, the two code
+    // buffers of the softmax part of the dlogits [R x V_pad] u8 each, the group
+    // scales [nc32] f32 and the sorted (token, slot) keys [R] u64
+    size_t rmax, qa, qb, gmax, keys;
     int S, nps;      // forward-only path: vocabulary splits, N-tiles per split (partials by row)
     int Sc, npsc;    // chunked path: vocabulary splits, N-tiles per split (partials by chunk slot)
     int n_ntiles;    // ceil(V / kBN)
@@ -81,6 +90,7 @@ struct WsLayout {
 };
 
 bool ws_layout(const grpo_shape& s, WsLayout* out);
+inline bool is_fp8(grpo_dtype t) { return t == GRPO_E4M3 || t == GRPO_E5M2; }
 
 // Forward logits + streaming logsumexp.  Two row sources:
 //   tiles != nullptr : forward row tiles over h_pol / h_ref (runs of masked-in rows)
@@ -123,6 +133,17 @@ struct ChunkParams {
     int* sched;             // zeroed work counter of this launch
     int* found_inf;
     int* status;
+    // 8-bit backward: P = g * softmax (the dlogits without their one-hot part) as
+    // 8-bit codes, scaled per row (qa, for dH) and per 32-column group (qb, for dW)
+    uint8_t* qa;            // [R x V_pad]  P * 448 / (|g| max_v softmax) of the row
+    uint8_t* qb;            // [R x V_pad]  P * 448 / gmax[group]
+    const float* rmax;      // [N] row maximum of the policy logits
+    float* gmax;            // [nc32] max over the chunk's rows of |P| bounds per 32-column group
+    unsigned long long* keys;   // [R] (token << 32 | slot) of the chunk's rows, ascending
+    const uint8_t* hq;      // compact 8-bit h_pol rows of the chunk [R x d]
+    const uint8_t* wq;      // 8-bit W [V x d]
+    float scale_h, scale_w; // per-tensor scales of the 8-bit h_pol and W
+    int e5m2;               // code format: E5M2 (1) or E4M3 (0)
 };
 
 struct MergeParams {
@@ -146,6 +167,7 @@ struct MergeParams {
     float* ell;
     float* row_stats;
     int* status;
+    float* rmax;            // nullable: row maximum of the policy logits (the 8-bit backward)
 };
 
 // ---- launches (return cudaError_t of the launch) ----
@@ -171,6 +193,10 @@ cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc
 cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, int sm_count, cudaStream_t st);
 cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, int sm_count, cudaStream_t st);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, int sm_count, cudaStream_t st);
+// 8-bit backward: group bounds, dlogit codes, sorted token keys, and the two GEMMs
+cudaError_t launch_f8_group_max(const ChunkParams& p, int sm_count, cudaStream_t st);
+cudaError_t launch_transform_f8(const ChunkParams& p, int sm_count, cudaStream_t st);
+cudaError_t launch_sort_keys(const ChunkParams& p, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cudaStream_t st);
 #ifdef GRPO_DEVICE_CHECKS
@@ -187,5 +213,9 @@ cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const C
                            bool bf16, cudaStream_t st);
 cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
                            bool bf16, cudaStream_t st);
+cudaError_t launch_dh_pair_fp8(const ChunkParams& p, const CUtensorMap& mQa, const CUtensorMap& mWmn, int n_sm,
+                               cudaStream_t st);
+cudaError_t launch_dw_pair_fp8(const ChunkParams& p, const CUtensorMap& mQbmn, const CUtensorMap& mHqmn, int n_sm,
+                               cudaStream_t st);
 
 }  // namespace grpo

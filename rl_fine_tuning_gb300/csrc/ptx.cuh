@@ -158,12 +158,16 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool in_bf16
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// Instruction descriptor of kind::f8f6f4 with both operands E4M3 (format 0),
-// K-major, fp32 accumulation.
-__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, bool e5m2) {
+// Instruction descriptor of kind::f8f6f4 with both operands of one 8-bit
+// format (E4M3 = 0, E5M2 = 1), fp32 accumulation.  a_mn / b_mn: operand is
+// MN-major (else K-major); 8-bit operands may be either.
+__host__ __device__ constexpr uint32_t make_idesc_f8(int M, int N, bool e5m2, bool a_mn = false,
+                                                     bool b_mn = false) {
     return (1u << 4)                                   // D: f32
            | ((e5m2 ? 1u : 0u) << 7)                   // A: E4M3 (0) or E5M2 (1)
            | ((e5m2 ? 1u : 0u) << 10)                  // B: the same format
+           | ((a_mn ? 1u : 0u) << 15)                  // A major
+           | ((b_mn ? 1u : 0u) << 16)                  // B major
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

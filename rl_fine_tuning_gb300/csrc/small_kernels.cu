@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 
@@ -233,7 +234,7 @@ cudaError_t launch_index(const uint8_t* mask, int64_t N, int R_max, int* counts,
 // combined across the warp in a fixed butterfly order.  Lane 0's results are
 // the ones used (every lane combines in its own order).
 __device__ __forceinline__ void merge_lse_warp(const float4* __restrict__ part, int S, int lane, float* lse_pol,
-                                               float* lse_ref) {
+                                               float* lse_ref, float* max_pol) {
     float mp = -INFINITY, mr = -INFINITY;
     for (int k = lane; k < S; k += 32) {
         const float4 ps = part[k];
@@ -258,6 +259,7 @@ __device__ __forceinline__ void merge_lse_warp(const float4* __restrict__ part, 
     }
     *lse_pol = mp + logf(sp);
     *lse_ref = mr + logf(sr);
+    *max_pol = mp;
 }
 
 // Per row: merge the per-split (max, sum-exp) partials of the policy and the
@@ -286,13 +288,13 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
         if (!GRPO_DCHECK(t >= 0 && t < p.N, p.status)) return;   // uniform across the warp
     }
     // t is uniform across the warp from here on
-    float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, pen = 0.f, g = 0.f, ell = 0.f;
+    float lse_p = 0.f, lse_r = 0.f, q = 0.f, p_ = 0.f, pen = 0.f, g = 0.f, ell = 0.f, zmax = 0.f;
     if (p.mask[t]) {
         const int tok = p.tokens[t];
         if (tok < 0 || tok >= p.V) {
             if (lane == 0) atomicCAS(p.status, 0, GRPO_ERR_SHAPE);
         } else {
-            merge_lse_warp(p.part + pidx * p.S, p.S, lane, &lse_p, &lse_r);
+            merge_lse_warp(p.part + pidx * p.S, p.S, lane, &lse_p, &lse_r, &zmax);
             const float2 z = p.zt[t];
             q = z.x - lse_p;
             p_ = z.y - lse_r;
@@ -344,6 +346,7 @@ __global__ void __launch_bounds__(kMergeThreads) k_merge(const MergeParams p) {
     p.lse[t] = lse_p;
     p.gco[t] = g;
     p.ell[t] = ell;
+    if (p.rmax) p.rmax[t] = zmax;
     if (p.row_stats) {
         float* o = p.row_stats + t * 5;
         o[0] = lse_p;
@@ -637,6 +640,172 @@ cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, int sm_coun
         k_transform<true><<<blocks, kTransformThreads, 0, st>>>(p, R);
     else
         k_transform<false><<<blocks, kTransformThreads, 0, st>>>(p, R);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ 8-bit backward
+// The dlogits of a row are dS = g (onehot(tok) - softmax).  The 8-bit backward
+// keeps the one-hot part exact (the GEMM epilogues add it) and sends only
+// P = g * softmax through 8-bit codes.  |P| <= |g| exp(m_grp - lse) for every
+// column of a 32-column group whose running max is m_grp, and the row's
+// largest |P| is |g| exp(max z - lse).
+
+// gmax[grp] = max over the chunk's rows of |g| exp(m_grp - lse): one bound of
+// |P| per 32-column group, shared by all rows of the chunk (zeroed
+// beforehand; non-negative floats order like their bit patterns).
+constexpr int kF8GroupRows = 64;
+
+__global__ void __launch_bounds__(256) k_f8_group_max(const ChunkParams p) {
+    if (p.chunk >= p.counts[C_NCHUNKS]) return;
+    const int rc = p.counts[C_CHUNK_ROWS];
+    const int c0 = p.chunk * rc;
+    const int n_c = min(rc, p.counts[C_NVALID] - c0);
+    const int s0 = blockIdx.x * kF8GroupRows;
+    if (s0 >= n_c) return;
+    const int s1 = min(n_c, s0 + kF8GroupRows);
+    const int ng = (p.V + 31) / 32;
+    for (int grp = threadIdx.x; grp < ng; grp += blockDim.x) {
+        float m = 0.f;
+        for (int slot = s0; slot < s1; ++slot) {
+            const int t = p.rows[c0 + slot];
+            if (!GRPO_DCHECK(t >= 0 && t < p.N && slot < p.R, p.status)) continue;
+            const float b = fabsf(p.gco[t]) * expf(p.mx[static_cast<int64_t>(slot) * p.nc32 + grp] - p.lse[t]);
+            m = fmaxf(m, b);
+        }
+        atomicMax(reinterpret_cast<int*>(p.gmax) + grp, __float_as_int(m));
+    }
+}
+
+cudaError_t launch_f8_group_max(const ChunkParams& p, int sm_count, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(p.gmax, 0, static_cast<size_t>(p.nc32) * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    int blocks = (p.R + kF8GroupRows - 1) / kF8GroupRows;
+    if (blocks < 1) blocks = 1;
+    (void)sm_count;
+    k_f8_group_max<<<blocks, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// two 8-bit codes of x0 (low byte) and x1 (high byte), saturating
+__device__ __forceinline__ uint32_t f8x2(float x0, float x1, bool e5m2) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, e5m2 ? __NV_E5M2 : __NV_E4M3));
+}
+
+// In place of the 16-bit dlogits pass: from the kept exponentials e = exp(z -
+// m_grp) (bf16) write the codes of P = g e exp(m_grp - lse) twice,
+//   qa = P * 448 / (|g| exp(zmax - lse)) = sign(g) 448 e exp(m_grp - zmax)   (per row)
+//   qb = P * 448 / gmax[grp]                                                 (per group)
+// Columns past V and rows past the chunk's last (to the next multiple of 128)
+// get code 0.
+__global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkParams p) {
+    if (p.chunk >= p.counts[C_NCHUNKS]) return;
+    const int rc = p.counts[C_CHUNK_ROWS];
+    const int c0 = p.chunk * rc;
+    const int n_c = min(rc, p.counts[C_NVALID] - c0);
+    const int n_fill = min(p.R, (n_c + kBM - 1) / kBM * kBM);
+    const int nvec = p.V_pad / 8;   // 8 columns per step: 16 bytes of exponentials, 8 bytes of each code
+    const bool e5 = p.e5m2 != 0;
+    for (int slot = blockIdx.x; slot < n_fill; slot += gridDim.x) {
+        const uint4* erow = reinterpret_cast<const uint4*>(p.dS + static_cast<int64_t>(slot) * p.V_pad);
+        uint2* arow = reinterpret_cast<uint2*>(p.qa + static_cast<int64_t>(slot) * p.V_pad);
+        uint2* brow = reinterpret_cast<uint2*>(p.qb + static_cast<int64_t>(slot) * p.V_pad);
+        if (slot >= n_c) {
+            for (int i = threadIdx.x; i < nvec; i += kTransformThreads) {
+                arow[i] = make_uint2(0, 0);
+                brow[i] = make_uint2(0, 0);
+            }
+            continue;
+        }
+        const int t = p.rows[c0 + slot];
+        if (!GRPO_DCHECK(t >= 0 && t < p.N, p.status)) continue;
+        const float g = p.gco[t];
+        const float lse = p.lse[t];
+        const float zmax = p.rmax[t];
+        const float sa = g == 0.f ? 0.f : copysignf(448.f, g);
+        const float* mrow = p.mx + static_cast<int64_t>(slot) * p.nc32;
+        for (int i = threadIdx.x; i < nvec; i += kTransformThreads) {
+            const int v0 = i * 8;
+            const int grp = v0 >> 5;
+            float ca = 0.f, cb = 0.f;
+            if (v0 < p.V) {
+                const float m = mrow[grp];
+                ca = sa * expf(m - zmax);
+                const float gm = p.gmax[grp];
+                cb = gm > 0.f ? g * expf(m - lse) * (448.f / gm) : 0.f;
+            }
+            const uint4 u = erow[i];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+            uint32_t oa[4], ob[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float e0 = __uint_as_float(w[j] << 16);
+                float e1 = __uint_as_float(w[j] & 0xFFFF0000u);
+                if (v0 + 2 * j >= p.V) e0 = 0.f;
+                if (v0 + 2 * j + 1 >= p.V) e1 = 0.f;
+                oa[j] = f8x2(ca * e0, ca * e1, e5);
+                ob[j] = f8x2(cb * e0, cb * e1, e5);
+            }
+            arow[i] = make_uint2(oa[0] | (oa[1] << 16), oa[2] | (oa[3] << 16));
+            brow[i] = make_uint2(ob[0] | (ob[1] << 16), ob[2] | (ob[3] << 16));
+        }
+    }
+}
+
+cudaError_t launch_transform_f8(const ChunkParams& p, int sm_count, cudaStream_t st) {
+    int blocks = p.R;
+    if (blocks > sm_count * 8) blocks = sm_count * 8;
+    k_transform_f8<<<blocks, kTransformThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// The chunk's (token << 32 | slot) keys in ascending order, by a bitonic sort
+// of the next power of two >= R keys in one block's shared memory (padding
+// keys sort last).  The dW epilogue finds the rows of a vocabulary row in it.
+__global__ void __launch_bounds__(1024) k_sort_keys(const ChunkParams p, int n_pow2) {
+    extern __shared__ unsigned long long keys_sh[];
+    if (p.chunk >= p.counts[C_NCHUNKS]) return;
+    const int rc = p.counts[C_CHUNK_ROWS];
+    const int c0 = p.chunk * rc;
+    const int n_c = min(rc, p.counts[C_NVALID] - c0);
+    for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+        unsigned long long k = ~0ull;
+        if (i < n_c) {
+            const int t = p.rows[c0 + i];
+            const int tok = GRPO_DCHECK(t >= 0 && t < p.N, p.status) ? p.tokens[t] : 0;
+            k = (static_cast<unsigned long long>(static_cast<uint32_t>(tok)) << 32) | static_cast<uint32_t>(i);
+        }
+        keys_sh[i] = k;
+    }
+    __syncthreads();
+    for (int size = 2; size <= n_pow2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool up = (i & size) == 0;
+                    const unsigned long long a = keys_sh[i], b = keys_sh[j];
+                    if ((a > b) == up) {
+                        keys_sh[i] = b;
+                        keys_sh[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < n_c && i < p.R; i += blockDim.x) p.keys[i] = keys_sh[i];
+}
+
+cudaError_t launch_sort_keys(const ChunkParams& p, cudaStream_t st) {
+    int n_pow2 = 1;
+    while (n_pow2 < p.R) n_pow2 <<= 1;
+    if (n_pow2 > kF8SortMax) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(n_pow2) * sizeof(unsigned long long);
+    cudaError_t e = cudaFuncSetAttribute(k_sort_keys, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_sort_keys<<<1, 1024, smem, st>>>(p, n_pow2);
     return cudaGetLastError();
 }
 

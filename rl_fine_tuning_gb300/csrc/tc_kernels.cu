@@ -32,6 +32,7 @@
 #include <cmath>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -829,6 +830,214 @@ struct DwPairT {
     __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
 };
 
+// ---------------------------------------------------------------------- 8-bit backward
+// The two backward GEMMs on 8-bit codes (kind::f8f6f4, M = 256 pairs, K = 32
+// per instruction, a K-stage of 128).  A operand: the codes of P = g softmax
+// (the dlogits without their one-hot part); B: the 8-bit W (dH) or the
+// chunk's 8-bit h_pol rows (dW).  Each code buffer carries one scale per
+// M-row (per dlogit row for dH, per 32-vocabulary-row group for dW), which
+// factors out of the K sum; the epilogue applies it and adds the one-hot part
+// exactly, from the decoded 8-bit inputs:
+//   dH_t = w scale_w (g_t Wc[tok_t] - s_t acc),           s_t = |g_t| exp(zmax_t - lse_t) / 448
+//   dW_v = w scale_h (sum_{t: tok_t = v} g_t hc_t - gmax_grp(v) / 448 acc)
+
+// MN-major 8-bit operand: [128 K-rows][128 MN-bytes] boxes of 16 KB; 8-K-row
+// groups 1024 B apart (SBO); K sub-step of 32 = +4096 B.
+__device__ __forceinline__ uint64_t desc_mnmajor_f8(uint32_t a) { return make_sdesc_sw128(a, 16384, 1024); }
+
+// 32 8-bit codes -> floats (exact)
+__device__ __forceinline__ void decode32_f8(const uint8_t* src, bool e5m2, float (&out)[32]) {
+    const uint4* q = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint4 u = q[h];
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const __nv_fp8x2_storage_t pr = static_cast<__nv_fp8x2_storage_t>((w[j] >> (16 * k)) & 0xFFFFu);
+                const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pr, e5m2 ? __NV_E5M2 : __NV_E4M3);
+                const float2 f = __half22float2(__half2(hr));
+                out[16 * h + 4 * j + 2 * k] = f.x;
+                out[16 * h + 4 * j + 2 * k + 1] = f.y;
+            }
+        }
+    }
+}
+
+struct DhPairF8T : DhPairT {
+    static constexpr int kStageElems = 128;
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!DhPairT::setup(p, sc)) return false;
+        sc.ks = (p.V + kStageElems - 1) / kStageElems;
+        return true;
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
+        return 2 * 16384 + 16384 * min(2, (p.d - c.n0) / 128);
+    }
+    __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(mA, bar, st, k * kStageElems, c.m0);
+        const int col = c.n0 + rank * 128;
+        if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384, col, k * kStageElems);
+    }
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        // the format is a launch parameter: E4M3 here, E5M2 in DhPairF8T5
+        mma_fmt<false>(st, acc, first);
+    }
+    template <bool kE5M2>
+    __device__ static void mma_fmt(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f8(256, 256, kE5M2, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_pair_f8(acc, desc_kmajor(st + kk * 32), desc_mnmajor_f8(st + 16384 + kk * 4096), idesc,
+                         (first && kk == 0) ? 0u : 1u);
+    }
+    template <bool>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int slot = mtile(sc, unit, rank) * kBM + row;
+        const int n0 = dtile(sc, unit) * kBN;
+        bool valid = slot < sc.n_c;
+        if (!__any_sync(0xffffffffu, valid)) return;
+        const int t = valid ? p.rows[sc.c0 + slot] : 0;
+        if (valid && !GRPO_DCHECK(t >= 0 && t < p.N, p.status)) valid = false;
+        // a token id outside [0, V) has g = 0 (the merge reported it): no W row is read for it
+        int tok = valid ? p.tokens[t] : 0;
+        const bool tok_ok = tok >= 0 && tok < p.V;
+        if (!tok_ok) tok = 0;
+        const float g = valid && tok_ok ? p.gco[t] : 0.f;
+        const float s_t = valid ? fabsf(g) * expf(p.rmax[t] - p.lse[t]) * (1.f / 448.f) : 0.f;
+        const float f = sc.winv * p.scale_w;
+        uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
+        const uint8_t* wrow = p.wq + static_cast<int64_t>(tok) * p.d;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            if (!valid) continue;
+            float wt[32];
+            decode32_f8(wrow + col0, p.e5m2 != 0, wt);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+                pk[j / 2] = pack2(f * (g * wt[j] - s_t * v[j]), f * (g * wt[j + 1] - s_t * v[j + 1]), true);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                st_global_v8(out + col0 + 16 * h, pk[8 * h], pk[8 * h + 1], pk[8 * h + 2], pk[8 * h + 3],
+                             pk[8 * h + 4], pk[8 * h + 5], pk[8 * h + 6], pk[8 * h + 7]);
+        }
+    }
+};
+
+struct DhPairF8T5 : DhPairF8T {
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        mma_fmt<true>(st, acc, first);
+    }
+};
+
+struct DwPairF8T : DwPairT {
+    static constexpr int kStageElems = 128;
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!DwPairT::setup(p, sc)) return false;
+        sc.ks = (sc.n_c + kStageElems - 1) / kStageElems;
+        return true;
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
+        return 2 * 16384 + 16384 * min(2, (p.d - c.n0) / 128);
+    }
+    __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(mA, bar, st, c.v0, k * kStageElems);
+        const int col = c.n0 + rank * 128;
+        if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384, col, k * kStageElems);
+    }
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        mma_fmt<false>(st, acc, first);
+    }
+    template <bool kE5M2>
+    __device__ static void mma_fmt(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f8(256, 256, kE5M2, true, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            umma_pair_f8(acc, desc_mnmajor_f8(st + kk * 4096), desc_mnmajor_f8(st + 16384 + kk * 4096), idesc,
+                         (first && kk == 0) ? 0u : 1u);
+    }
+    template <bool>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int v = vtile(sc, unit, rank) * kBM + row;
+        const int n0 = dtile(sc, unit) * kBN;
+        const bool valid = v < p.V;
+        if (!__any_sync(0xffffffffu, valid)) return;
+        const bool first_chunk = p.chunk == 0;
+        // the chunk's rows whose sampled token is v: a run of the sorted keys
+        int lo = 0, hi = sc.n_c;
+        const unsigned long long key = static_cast<unsigned long long>(static_cast<uint32_t>(valid ? v : 0)) << 32;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (p.keys[mid] < key) lo = mid + 1;
+            else hi = mid;
+        }
+        int n_hit = 0;
+        while (valid && lo + n_hit < sc.n_c && (p.keys[lo + n_hit] >> 32) == static_cast<unsigned long long>(v))
+            ++n_hit;
+        const float fb = valid ? p.gmax[v >> 5] * (1.f / 448.f) : 0.f;
+        const float f = sc.winv * p.scale_h;
+        float* out = p.dW + static_cast<int64_t>(valid ? v : 0) * p.d;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float x[32];
+            tmem_ld32(tacc + c * 32, x);
+            if (!valid) continue;
+            float oh[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) oh[j] = 0.f;
+            for (int h = 0; h < n_hit; ++h) {
+                const int slot = static_cast<int>(p.keys[lo + h] & 0xFFFFFFFFull);
+                const int t = p.rows[sc.c0 + slot];
+                if (!GRPO_DCHECK(slot < p.R && t >= 0 && t < p.N, p.status)) continue;
+                const float g = p.gco[t];
+                float hv[32];
+                decode32_f8(p.hq + static_cast<int64_t>(slot) * p.d + col0, p.e5m2 != 0, hv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) oh[j] = fmaf(g, hv[j], oh[j]);
+            }
+            float* o = out + col0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float r[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[i] = f * (oh[8 * j + i] - fb * x[8 * j + i]);
+                if (!first_chunk) {
+                    float prev[8];
+                    ld_global_v8(o + 8 * j, prev);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) r[i] += prev[i];
+                }
+                st_global_v8(o + 8 * j, __float_as_uint(r[0]), __float_as_uint(r[1]), __float_as_uint(r[2]),
+                             __float_as_uint(r[3]), __float_as_uint(r[4]), __float_as_uint(r[5]),
+                             __float_as_uint(r[6]), __float_as_uint(r[7]));
+            }
+        }
+    }
+};
+
+struct DwPairF8T5 : DwPairF8T {
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        mma_fmt<true>(st, acc, first);
+    }
+};
+
 template <class T, bool kBf16>
 __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const CUtensorMap& mA, const CUtensorMap& mA2,
                                              const CUtensorMap& mB) {
@@ -1038,6 +1247,10 @@ GRPO_PAIR_KERNEL(grpo_fwd_pair_e4m3_kernel, FwdPairF8T<false>)
 GRPO_PAIR_KERNEL(grpo_fwd_pair_e5m2_kernel, FwdPairF8T<true>)
 GRPO_PAIR_KERNEL(grpo_dh_pair_kernel, DhPairT)
 GRPO_PAIR_KERNEL(grpo_dw_pair_kernel, DwPairT)
+GRPO_PAIR_KERNEL(grpo_dh_pair_e4m3_kernel, DhPairF8T)
+GRPO_PAIR_KERNEL(grpo_dh_pair_e5m2_kernel, DhPairF8T5)
+GRPO_PAIR_KERNEL(grpo_dw_pair_e4m3_kernel, DwPairF8T)
+GRPO_PAIR_KERNEL(grpo_dw_pair_e5m2_kernel, DwPairF8T5)
 #undef GRPO_PAIR_KERNEL
 
 // Persistent launch: one CTA per SM, in clusters of kC; the grid is capped by
@@ -1093,6 +1306,18 @@ cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const
                            bool bf16, cudaStream_t st) {
     return bf16 ? launch_tc<DwPairT, 2>(grpo_dw_pair_kernel<true>, p, mDSmn, mDSmn, mHcmn, n_sm, st)
                 : launch_tc<DwPairT, 2>(grpo_dw_pair_kernel<false>, p, mDSmn, mDSmn, mHcmn, n_sm, st);
+}
+
+cudaError_t launch_dh_pair_fp8(const ChunkParams& p, const CUtensorMap& mQa, const CUtensorMap& mWmn, int n_sm,
+                               cudaStream_t st) {
+    return p.e5m2 ? launch_tc<DhPairF8T5, 2>(grpo_dh_pair_e5m2_kernel<true>, p, mQa, mQa, mWmn, n_sm, st)
+                  : launch_tc<DhPairF8T, 2>(grpo_dh_pair_e4m3_kernel<true>, p, mQa, mQa, mWmn, n_sm, st);
+}
+
+cudaError_t launch_dw_pair_fp8(const ChunkParams& p, const CUtensorMap& mQbmn, const CUtensorMap& mHqmn, int n_sm,
+                               cudaStream_t st) {
+    return p.e5m2 ? launch_tc<DwPairF8T5, 2>(grpo_dw_pair_e5m2_kernel<true>, p, mQbmn, mQbmn, mHqmn, n_sm, st)
+                  : launch_tc<DwPairF8T, 2>(grpo_dw_pair_e4m3_kernel<true>, p, mQbmn, mQbmn, mHqmn, n_sm, st);
 }
 
 cudaError_t launch_fwd(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr, const CUtensorMap& mW,

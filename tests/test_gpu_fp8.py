@@ -1,7 +1,10 @@
-"""The 8-bit forward (grpo_loss_fwd_fp8, E4M3 and E5M2 inputs) against the
-fp64 oracle on the same 8-bit inputs: the oracle reads every code times its
-tensor's scale exactly in fp64, so this is the same parity bar as the 16-bit
-forward."""
+"""The 8-bit entry points (E4M3 and E5M2 inputs) against the fp64 oracle on
+the same 8-bit inputs: the oracle reads every code times its tensor's scale
+exactly in fp64.  The forward (grpo_loss_fwd_fp8) meets the bar of the 16-bit
+forward.  The forward+backward (grpo_loss_fwd_bwd_fp8) is held to the 16-bit
+tolerances too (loss relative 1e-3, dH and dW 2e-2 x max|ref|) against the
+exact gradient of the decoded inputs: its 8-bit dlogits carry only the
+softmax part of each row, the one-hot part being added exactly."""
 import numpy as np
 import pytest
 
@@ -91,3 +94,89 @@ def test_fp8_forward_full_size_sampled_rows(fmt):
     A = exp["adv"][rows // cfg.L].astype(np.float64)
     ell = -A + cfg.beta * res["row_stats"][rows, 4]
     assert abs(res["loss"] - ell.mean()) <= 1e-5 * max(1e-3, abs(ell.mean()))
+
+
+def run_fp8_bwd(wl8, mask=None, chunk_rows=0):
+    cfg = wl8.cfg
+    s_pol, s_ref, s_w = wl8.extra["scales"]
+    dtype = rg.E5M2 if wl8.extra.get("fp8") == "e5m2" else rg.E4M3
+    shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, dtype, beta=cfg.beta, eps=cfg.eps,
+                          chunk_rows=chunk_rows)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
+    h_pol, h_ref, W = dev(wl8.h_pol), dev(wl8.h_ref), dev(wl8.W)
+    tokens, lengths, rewards = dev(wl8.tokens), dev(wl8.lengths), dev(wl8.rewards)
+    adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
+    rg.grpo_group_advantages(rewards, cfg.n_groups, cfg.G, cfg.eps, True, adv)
+    if mask is None:
+        m = torch.empty(cfg.N, dtype=torch.uint8, device="cuda")
+        rg.grpo_build_mask(lengths, shape, m)
+    else:
+        m = dev(mask.astype(np.uint8))
+    ws = torch.empty(rg.grpo_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    stats = torch.zeros((cfg.N, 5), dtype=torch.float32, device="cuda")
+    status = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    # sentinels: every element must be written (masked dH rows with 0)
+    dH = torch.full((cfg.N, cfg.d), 7.0, dtype=torch.bfloat16, device="cuda")
+    dW = torch.full((cfg.V, cfg.d), 7.0, dtype=torch.float32, device="cuda")
+    rg.grpo_loss_fwd_bwd_fp8(h_pol, h_ref, W, s_pol, s_ref, s_w, tokens, m, adv, shape, ws, loss, dH, dW, stats,
+                             status)
+    torch.cuda.synchronize()
+    res = dict(loss=float(loss.item()), status=int(status.item()), row_stats=stats.cpu().numpy().astype(np.float64),
+               adv=adv.cpu().numpy(), mask=m.cpu().numpy(), dH=dH.float().cpu().numpy().astype(np.float64),
+               dW=dW.cpu().numpy().astype(np.float64))
+    exp = oracle.expected(oracle.dequantized_workload(wl8), mask=res["mask"])
+    return res, exp
+
+
+def assert_fp8_grad_parity(res, exp):
+    assert_fwd_parity(res, exp)
+    rows = exp["eval_rows"]
+    err_h = np.abs(res["dH"][rows] - exp["dH"]).max()
+    assert err_h <= 2e-2 * np.abs(exp["dH"]).max(), ("dH", err_h, np.abs(exp["dH"]).max())
+    masked = np.flatnonzero(exp["mask"] == 0)
+    assert np.all(res["dH"][masked] == 0)
+    err_w = np.abs(res["dW"] - exp["dW"]).max()
+    assert err_w <= 2e-2 * np.abs(exp["dW"]).max(), ("dW", err_w, np.abs(exp["dW"]).max())
+    return err_h / np.abs(exp["dH"]).max(), err_w / np.abs(exp["dW"]).max()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("over,chunk_rows", [
+    (dict(), 0),
+    (dict(G=4, L=500, d=384, V=3000, len_lo=1, len_hi=500), 256),          # ragged V, several chunks
+    (dict(G=4, L=256, d=256, V=200, len_lo=64, len_hi=256), 128),          # many rows per token in a chunk
+    (dict(G=2, L=300, d=256, V=777, sigma_ref=0.4), 0),                    # a KL large enough to matter
+])
+def test_fp8_forward_backward_parity(over, chunk_rows, fmt):
+    cfg = synth.make_config("tiny", **over)
+    res, exp = run_fp8_bwd(synth.generate_fp8(cfg, seed=43, fmt=fmt), chunk_rows=chunk_rows)
+    assert np.array_equal(res["adv"].view(np.uint32), exp["adv"].view(np.uint32))
+    assert_fp8_grad_parity(res, exp)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_forward_backward_full_shape_submask(fmt):
+    # the Llama-3.1-8B head shape with 400 masked-in rows in four runs, 128-row chunks
+    cfg = synth.CONFIGS["llama-3.1-8b-head"]
+    wl8 = synth.generate_fp8(cfg, seed=0, fmt=fmt)
+    rng = np.random.default_rng(17)
+    live = list(np.flatnonzero(wl8.lengths >= 270))
+    mask = np.zeros(cfg.N, np.uint8)
+    for run in (1, 9, 130, 260):
+        i = int(rng.choice(live))
+        live.remove(i)
+        j = int(rng.integers(0, wl8.lengths[i] - run + 1))
+        mask[i * cfg.L + j: i * cfg.L + j + run] = 1
+    res, exp = run_fp8_bwd(wl8, mask=mask, chunk_rows=128)
+    assert_fp8_grad_parity(res, exp)
+
+
+def test_fp8_backward_forward_loss_equals_the_forward_entry_point():
+    cfg = synth.make_config("tiny", G=4, L=300, d=256, V=1500, len_lo=1, len_hi=300)
+    wl8 = synth.generate_fp8(cfg, seed=44, fmt="e4m3")
+    res_b, _ = run_fp8_bwd(wl8)
+    res_f, _ = run_fp8(wl8)
+    assert res_b["status"] == 0 and res_f["status"] == 0
+    assert res_b["loss"] == res_f["loss"]
+    assert np.array_equal(res_b["row_stats"], res_f["row_stats"])
