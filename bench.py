@@ -704,8 +704,16 @@ def run_forward_modes(args, ranks):
             torch.cuda.synchronize()
             ms = e0.elapsed_time(e1) / args.steps
             flops = 8.0 * n_valid * cfg.V * cfg.d
+            # per-kernel breakdown from a second, instrumented pass
+            rg.grpo_profile_enable(True)
+            for _ in range(args.steps):
+                step_bwd()
+            torch.cuda.synchronize()
+            rg.grpo_profile_enable(False)
+            kern = {k: round(v[0] / args.steps, 3) for k, v in rg.grpo_profile_collect().items() if v[1]}
             out[mode + "_fwd_bwd"] = {"ms_per_step": ms, "tokens_per_s": n_valid / (ms / 1e3),
-                                      "tflops": flops / (ms / 1e3) / 1e12, "loss": float(loss.item())}
+                                      "tflops": flops / (ms / 1e3) / 1e12, "loss": float(loss.item()),
+                                      "kernel_ms_per_step": kern}
             del dH, dW
         del mats, ws, wl
         torch.cuda.empty_cache()
