@@ -237,6 +237,7 @@ bool ws_layout(const grpo_shape& s, WsLayout* o) {
     o->partc = take(static_cast<size_t>(o->R) * o->Sc * 16);
     o->mx = take(static_cast<size_t>(o->R) * o->nc32 * 4);
     o->ds = take(static_cast<size_t>(o->R) * o->V_pad * 2);
+    o->hct = take(static_cast<size_t>(o->R) * s.d * 2);
     o->rmax = o->qa = o->qb = o->gmax = o->keys = 0;
     if (is_fp8(s.dtype)) {
         // the 8-bit backward's buffers (its forward-only entry point needs none of them)
@@ -458,7 +459,7 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
                !make_map(&mW_mn, in.W, bf16, s.d, s.V, s.d, 64, kBK) ||
                !make_map(&mHc_k, hc, bf16, s.d, L.R, s.d, kBK, kBM) ||
                !make_map(&mHcr_k, hcr, bf16, s.d, L.R, s.d, kBK, kBM) ||
-               !make_map(&mHc_mn, hc, bf16, s.d, L.R, s.d, 64, kBK) ||
+               !make_map(&mHc_mn, w + L.hct, bf16, L.R, s.d, L.R, kBK, 128) ||
                !make_map(&mDS_k, ds, bf16, s.V, L.R, L.V_pad, kBK, kBM) ||
                !make_map(&mDS_mn, ds, bf16, s.V, L.R, L.V_pad, 64, kBK)) {
         return GRPO_ERR_LAUNCH;
@@ -529,7 +530,11 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
         if (f8 && bwd) mp.rmax = reinterpret_cast<float*>(w + L.rmax);
         if (launch(GRPO_PROF_GATHER, st, [&] {
-                return launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, row_bytes, dev.sm_count, st);
+                // 16-bit inputs with a backward also get the transposed compact h_pol rows (dW's B operand)
+                return bwd && !f8 ? launch_gather_rows_t(cp, in.h_pol, hc, in.h_ref, hcr, w + L.hct, L.R,
+                                                         dev.sm_count, st)
+                                  : launch_gather_rows(cp, in.h_pol, hc, in.h_ref, hcr, L.R, row_bytes, dev.sm_count,
+                                                       st);
             }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_FWD, st, [&] {

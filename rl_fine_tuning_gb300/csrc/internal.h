@@ -77,6 +77,7 @@ struct WsLayout {
     // buffers of the softmax part of the dlogits [R x V_pad] u8 each, the group
     // scales [nc32] f32 and the sorted (token, slot) keys [R] u64
     size_t rmax, qa, qb, gmax, keys;
+    size_t hct;      // the chunk's compact h_pol rows transposed, [d x R] 16-bit (dW's K-major B operand)
     int S, nps;      // forward-only path: vocabulary splits, N-tiles per split (partials by row)
     int Sc, npsc;    // chunked path: vocabulary splits, N-tiles per split (partials by chunk slot)
     int n_ntiles;    // ceil(V / kBN)
@@ -190,6 +191,9 @@ cudaError_t launch_loss_reduce(const float* ell, int64_t N, double* blocksum, in
 // The grid-stride kernels below size their grids in multiples of the device's SM count.
 cudaError_t launch_gather_rows(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr, int R,
                                int row_bytes, int sm_count, cudaStream_t st);
+// 16-bit inputs: the same gather, also writing the transpose of the compact h_pol rows
+cudaError_t launch_gather_rows_t(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr,
+                                 void* hct, int R, int sm_count, cudaStream_t st);
 cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, int sm_count, cudaStream_t st);
 cudaError_t launch_clear_grads(const int* counts, int* found_inf, float* dW, int64_t n, int sm_count, cudaStream_t st);
 cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void* dH, int sm_count, cudaStream_t st);

@@ -73,15 +73,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // After an abort, TMA loads that the CTA issued before its roles stopped may
-// still be writing into its shared memory.  In a CTA pair they complete on the
-// leader's barrier, which the issuing peer cannot observe, so the CTA cannot
-// wait for them one by one.  An issued load lands within microseconds: every
-// thread of an aborting CTA waits this long before the CTA leaves.
+// still be writing into its shared memory.  The kernels first wait for them on
+// the full barriers they complete on (see wait_inflight in tc_kernels.cu).
+// Where that cannot account for every issued load (in a CTA pair, one CTA
+// issued loads for a K-stage the other never armed), the CTA falls back to
+// this fixed wait: an issued load lands within microseconds.
 constexpr unsigned long long kAbortGraceNs = 200ull * 1000ull;   // 200 us
 
-// Call after the CTA's last __syncthreads, when the flag no longer changes.
-__device__ __forceinline__ void abort_grace(const volatile int* abort_flag) {
-    if (!*abort_flag) return;
+// Call after the CTA's last __syncthreads, when the flag no longer changes;
+// `any` also waits when this CTA's own flag is clear (its pair peer aborted).
+__device__ __forceinline__ void abort_grace(const volatile int* abort_flag, bool any = false) {
+    if (!*abort_flag && !any) return;
     const uint64_t t0 = globaltimer();
     while (globaltimer() - t0 < kAbortGraceNs) {
     }
@@ -243,6 +245,17 @@ __device__ __forceinline__ uint32_t map_cluster(uint32_t local_addr, uint32_t ra
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
     return r;
+}
+
+// 32-bit load / store of shared memory of a CTA of the cluster (cluster address)
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
 // arrive on an mbarrier of another CTA of the cluster (release at cluster scope)

@@ -541,6 +541,79 @@ __global__ void k_gather_rows(const int* __restrict__ counts, const int* __restr
     }
 }
 
+// The gather of 16-bit rows, one 64-row x 64-column tile per block iteration:
+// hc and hcr as above, and hct[k][slot] = hc[slot][k] ([d x R], pitch R) through
+// a shared-memory tile of 32-bit words (two columns each; 33 words per row, so
+// the column reads of the transposed write hit distinct banks up to 2-way).
+constexpr int kGatherTile = 64;
+
+__global__ void __launch_bounds__(256) k_gather_rows_t(const int* __restrict__ counts, const int* __restrict__ rows,
+                                                       int chunk, const uint4* __restrict__ h, uint4* __restrict__ hc,
+                                                       const uint4* __restrict__ hr, uint4* __restrict__ hcr,
+                                                       uint16_t* __restrict__ hct, int d, int R, int64_t N,
+                                                       int* status) {
+    __shared__ uint32_t tile[kGatherTile][kGatherTile / 2 + 1];
+    if (chunk >= counts[C_NCHUNKS]) return;
+    const int rc = counts[C_CHUNK_ROWS];
+    const int c0 = chunk * rc;
+    const int n_c = min(rc, counts[C_NVALID] - c0);
+    const int n_fill = min(R, (n_c + kBM - 1) / kBM * kBM);   // a multiple of 128
+    const int nt_d = d / kGatherTile;
+    const int n_tiles = (n_fill / kGatherTile) * nt_d;
+    const int vpr = d / 8;                                    // 16-byte vectors per row
+    for (int tix = blockIdx.x; tix < n_tiles; tix += gridDim.x) {
+        const int r0 = (tix / nt_d) * kGatherTile;
+        const int d0 = (tix % nt_d) * kGatherTile;
+        for (int i = threadIdx.x; i < kGatherTile * 8; i += blockDim.x) {
+            const int r = i >> 3, v = i & 7;
+            const int slot = r0 + r;
+            uint4 x = make_uint4(0, 0, 0, 0), y = make_uint4(0, 0, 0, 0);
+            if (slot < n_c) {
+                const int t = rows[c0 + slot];
+                if (GRPO_DCHECK(t >= 0 && t < N, status)) {
+                    const int64_t src = static_cast<int64_t>(t) * vpr + (d0 >> 3) + v;
+                    x = h[src];
+                    y = hr[src];
+                }
+            }
+            const int64_t dst = static_cast<int64_t>(slot) * vpr + (d0 >> 3) + v;
+            hc[dst] = x;
+            hcr[dst] = y;
+            tile[r][4 * v] = x.x;
+            tile[r][4 * v + 1] = x.y;
+            tile[r][4 * v + 2] = x.z;
+            tile[r][4 * v + 3] = x.w;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kGatherTile * 8; i += blockDim.x) {
+            const int k = i >> 3, v = i & 7;   // output row d0 + k, slots r0 + 8v .. r0 + 8v + 7
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t w0 = tile[8 * v + 2 * j][k >> 1], w1 = tile[8 * v + 2 * j + 1][k >> 1];
+                const uint32_t e0 = (k & 1) ? (w0 >> 16) : (w0 & 0xFFFFu);
+                const uint32_t e1 = (k & 1) ? (w1 >> 16) : (w1 & 0xFFFFu);
+                o[j] = e0 | (e1 << 16);
+            }
+            *reinterpret_cast<uint4*>(hct + static_cast<int64_t>(d0 + k) * R + r0 + 8 * v) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_gather_rows_t(const ChunkParams& p, const void* h_pol, void* hc, const void* h_ref, void* hcr,
+                                 void* hct, int R, int sm_count, cudaStream_t st) {
+    const int64_t tiles = static_cast<int64_t>(R / kGatherTile) * (p.d / kGatherTile);
+    int blocks = static_cast<int>(tiles < sm_count * 8 ? tiles : sm_count * 8);
+    if (blocks < 1) blocks = 1;
+    k_gather_rows_t<<<blocks, 256, 0, st>>>(p.counts, p.rows, p.chunk, static_cast<const uint4*>(h_pol),
+                                            static_cast<uint4*>(hc), static_cast<const uint4*>(h_ref),
+                                            static_cast<uint4*>(hcr), static_cast<uint16_t*>(hct), p.d, R, p.N,
+                                            p.status);
+    return cudaGetLastError();
+}
+
 #ifdef GRPO_DEVICE_CHECKS
 // One thread stores one past the end of a 16-element shared array through the
 // checked access pattern of the kernels: the check refuses the store and

@@ -14,7 +14,8 @@
 //   grpo_fwd_pair_e4m3_kernel, grpo_fwd_pair_e5m2_kernel  the same forward
 //         on 8-bit inputs (kind::f8f6f4), scaled by the per-tensor scales.
 //   grpo_dh_pair_kernel   dH[rows] = (1/N_valid) * dlogits . W        (K = vocabulary)
-//   grpo_dw_pair_kernel   dW      += (1/N_valid) * dlogits^T . H_pol  (K = chunk rows)
+//   grpo_dw_pair_kernel   dW      += (1/N_valid) * dlogits^T . H_pol  (K = chunk rows; H_pol from
+//         the transposed compact rows, so its operand is K-major)
 // Single-SM kernel (tcgen05.mma.cta_group::1, M = 128):
 //   grpo_fwd_lse_kernel   the forward over row tiles of h_pol / h_ref (the
 //         workspace-free entry point), policy and reference MMAs sharing B.
@@ -67,6 +68,9 @@ struct Smem {
     uint32_t* tmem_slot;
     volatile int* abort_flag;
     volatile int* unit_id;
+    // [0] K-stages whose TMA loads this CTA's producer issued, [1] K-stages the
+    // MMA lane consumed, [2] 1 once every issued load is known to have landed
+    volatile int* ld_count;
 };
 
 template <int kStages, int kStageBytes>
@@ -85,12 +89,30 @@ __device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
     s.tmem_slot = reinterpret_cast<uint32_t*>(s.unit_empty + kUnitSlots);
     s.abort_flag = reinterpret_cast<volatile int*>(s.tmem_slot + 1);
     s.unit_id = s.abort_flag + 1;
+    s.ld_count = s.unit_id + kUnitSlots;
     return s;
 }
 
 template <class T>
 constexpr int smem_bytes() {
-    return T::kStages * T::kStageBytes + 1024 + 256;
+    return T::kStages * T::kStageBytes + 1024 + 512;
+}
+
+// After an abort, wait (at most kInflightNs in all) for the K-stages whose loads
+// were issued but not consumed, phases used .. issued-1 of the full barriers,
+// to complete.  Returns true when all of them did.
+constexpr unsigned long long kInflightNs = 2ull * 1000ull * 1000ull;   // 2 ms
+
+template <int kStages>
+__device__ __forceinline__ bool wait_inflight(uint64_t* full, int used, int issued) {
+    const uint64_t t0 = globaltimer();
+    for (int i = used; i < issued; ++i) {
+        const uint32_t a = smem_u32(&full[i % kStages]);
+        const uint32_t parity = static_cast<uint32_t>(i / kStages) & 1u;
+        while (!mbar_try_wait(a, parity))
+            if (globaltimer() - t0 > kInflightNs) return false;
+    }
+    return true;
 }
 
 __device__ __forceinline__ uint16_t f32_to_16(float x, bool bf16) {
@@ -277,6 +299,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
         }
         mbar_init(sm.drain, 1);
         *sm.abort_flag = 0;
+        sm.ld_count[0] = sm.ld_count[1] = sm.ld_count[2] = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -296,7 +319,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int s = 0, us = 0;
+            int s = 0, us = 0, n_issued = 0;
             uint32_t ph = 0, uph = 0;
             while (true) {
                 const int unit = atomicAdd(sched, 1);
@@ -319,6 +342,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
                         uint8_t* st = sm.stages + s * T::kStageBytes;
                         mbar_arrive_expect_tx(&sm.full[s], bytes);
                         T::load(p, sc, c, k, st, &sm.full[s], &mA, &mA2, &mB);
+                        ++n_issued;
                         if (++s == T::kStages) {
                             s = 0;
                             ph ^= 1u;
@@ -326,12 +350,13 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
                     }
                 }
             }
-        producer_done:;
+        producer_done:
+            sm.ld_count[0] = n_issued;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            int s = 0, us = 0;
+            int s = 0, us = 0, n_used = 0;
             uint32_t ph = 0, uph = 0;
             int it = 0;
             while (true) {
@@ -353,6 +378,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
                     const uint32_t acc = tmem + b * T::kAccStride;
                     for (int k = 0; k < ks; ++k) {
                         if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, status)) goto mma_done;
+                        ++n_used;
                         tc_fence_after();
                         T::template mma<kBf16>(smem_u32(sm.stages + s * T::kStageBytes), acc, k == 0);
                         umma_commit(&sm.empty[s]);
@@ -365,6 +391,7 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
                 }
             }
         mma_done:
+            sm.ld_count[1] = n_used;
             // every issued MMA (and every commit it feeds) must have finished
             // before TMEM is released
             umma_commit(sm.drain);
@@ -416,7 +443,13 @@ __device__ __forceinline__ void tc_body(const typename T::Params& p, const CUten
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    abort_grace(sm.abort_flag);
+    // after an abort, the loads still in flight land on this CTA's own full barriers
+    if (*sm.abort_flag) {
+        if (threadIdx.x == 0)
+            sm.ld_count[2] = wait_inflight<T::kStages>(sm.full, sm.ld_count[1], sm.ld_count[0]) ? 1 : 0;
+        __syncthreads();
+        if (!sm.ld_count[2]) abort_grace(sm.abort_flag);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -729,7 +762,7 @@ struct DhPairT {
 
 struct DwPairT {
     static constexpr int kStages = 7;
-    static constexpr int kStageBytes = 16384 + 16384;   // A (64 slots x 128 vocab), B half (64 slots x 128 d)
+    static constexpr int kStageBytes = 16384 + 16384;   // A (64 slots x 128 vocab), B half (128 d x 64 slots)
     using Params = ChunkParams;
     using Sched = ChunkSched;
     struct Coord {
@@ -766,24 +799,22 @@ struct DwPairT {
         return Coord{vtile(sc, unit, rank) * kBM, dtile(sc, unit) * kBN};
     }
     __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
-        return 2 * 16384 + 8192 * min(4, (p.d - c.n0) / 64);
+        return 2 * 16384 + 16384 * min(2, (p.d - c.n0 + 127) / 128);
     }
     __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
                                 const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
         tma_load_2d_pair(mA, bar, st, c.v0, k * kBK);
         tma_load_2d_pair(mA, bar, st + 8192, c.v0 + 64, k * kBK);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int col = c.n0 + rank * 128 + 64 * j;
-            if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384 + 8192 * j, col, k * kBK);
-        }
+        // B: 128 rows of the transposed compact h_pol (d) x 64 chunk slots (K), K-major
+        const int col = c.n0 + rank * 128;
+        if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384, k * kBK, col);
     }
     template <bool kBf16>
     __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
-        constexpr uint32_t idesc = make_idesc_f16(256, 256, kBf16, true, true);
+        constexpr uint32_t idesc = make_idesc_f16(256, 256, kBf16, true, false);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-            umma_pair_f16(acc, desc_mnmajor(st + kk * 2048), desc_mnmajor(st + 16384 + kk * 2048), idesc,
+            umma_pair_f16(acc, desc_mnmajor(st + kk * 2048), desc_kmajor(st + 16384 + kk * 32), idesc,
                           (first && kk == 0) ? 0u : 1u);
     }
     __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
@@ -1067,6 +1098,7 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
         }
         mbar_init(sm.drain, 1);
         *sm.abort_flag = 0;
+        sm.ld_count[0] = sm.ld_count[1] = sm.ld_count[2] = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -1089,7 +1121,7 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (both CTAs)
         if (lane == 0) {
-            int s = 0;
+            int s = 0, n_issued = 0;
             uint32_t ph = 0;
             for (int unit = cid; unit < sc.n_units; unit += n_pairs) {
                 const int n_items = T::items(p, sc, unit);
@@ -1101,6 +1133,7 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
                         if (!mbar_wait(&sm.empty[s], ph ^ 1u, sm.abort_flag, status)) goto producer_done;
                         if (leader) mbar_arrive_expect_tx(&sm.full[s], bytes);
                         T::load(p, sc, c, k, sm.stages + s * T::kStageBytes, full0 + 8u * s, &mA, &mA2, &mB, rank);
+                        ++n_issued;
                         if (++s == T::kStages) {
                             s = 0;
                             ph ^= 1u;
@@ -1108,12 +1141,13 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
                     }
                 }
             }
-        producer_done:;
+        producer_done:
+            sm.ld_count[0] = n_issued;
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader only)
         if (lane == 0 && leader) {
-            int s = 0;
+            int s = 0, n_used = 0;
             uint32_t ph = 0;
             int it = 0;
             for (int unit = cid; unit < sc.n_units; unit += n_pairs) {
@@ -1127,6 +1161,7 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
                     const uint32_t acc = tmem + b * 256;
                     for (int k = 0; k < ks; ++k) {
                         if (!mbar_wait(&sm.full[s], ph, sm.abort_flag, status)) goto mma_done;
+                        ++n_used;
                         tc_fence_after();
                         T::template mma<kBf16>(smem_u32(sm.stages + s * T::kStageBytes), acc, k == 0);
                         umma_pair_commit_both(&sm.empty[s]);
@@ -1139,6 +1174,7 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
                 }
             }
         mma_done:
+            sm.ld_count[1] = n_used;
             umma_pair_commit(sm.drain);
             {
                 const uint32_t a = smem_u32(sm.drain);
@@ -1183,10 +1219,30 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    abort_grace(sm.abort_flag);
+    // After an abort in either CTA, the loads still in flight (both CTAs' loads
+    // complete on the leader's full barriers) must land before either CTA leaves.
+    // The leader reads both CTAs' counts, waits for the K-stages both issued and
+    // its MMA did not consume, and tells both CTAs whether that covered every
+    // issued load; only when it did not do they fall back to the fixed wait.
+    cluster_sync();
+    if (leader && threadIdx.x == 0) {
+        const uint32_t peer_cnt = map_cluster(smem_u32(const_cast<int*>(sm.ld_count)), 1);
+        const uint32_t peer_abort = map_cluster(smem_u32(const_cast<int*>(sm.abort_flag)), 1);
+        const int peer_issued = static_cast<int>(ld_shared_cluster_u32(peer_cnt));
+        const bool aborted = *sm.abort_flag || ld_shared_cluster_u32(peer_abort) != 0;
+        int settled = 1;
+        if (aborted) {
+            const int issued = sm.ld_count[0], used = sm.ld_count[1];
+            const int both = min(issued, peer_issued);
+            settled = wait_inflight<T::kStages>(sm.full, used, both) && issued == peer_issued ? 1 : 0;
+        }
+        sm.ld_count[2] = settled;
+        st_shared_cluster_u32(peer_cnt + 8u, static_cast<uint32_t>(settled));
+    }
     // the leader's MMAs write the peer's tensor memory, and the peer's loads
     // complete on the leader's barriers: nobody leaves before both are done
     cluster_sync();
+    if (!sm.ld_count[2]) abort_grace(sm.abort_flag, true);
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem, kTmemCols);

@@ -96,9 +96,9 @@ def test_shape_defaults_and_workspace_bytes(lib):
     n = rg.grpo_workspace_bytes(s)
     N, R, V, d = 160000, 38 * 128, 128256, 4096
     assert rg.grpo_chunk_rows(s) == R      # d/256 = 16: 19 tile pairs x 16 d tiles = 4 x 76 dH units
-    # O(R*V + R*d + N) -- never O(N*V): dlogits chunk, two compact hidden-state chunks,
-    # per-32-column maxima, per-split partials, per-row arrays
-    assert R * V * 2 <= n < R * V * 2 + 2 * R * d * 2 + R * ((V + 31) // 32) * 4 + R * 256 * 16 + 300 * N + (1 << 20)
+    # O(R*V + R*d + N) -- never O(N*V): dlogits chunk, three compact hidden-state chunks (policy,
+    # reference, policy transposed), per-32-column maxima, per-split partials, per-row arrays
+    assert R * V * 2 <= n < R * V * 2 + 3 * R * d * 2 + R * ((V + 31) // 32) * 4 + R * 256 * 16 + 300 * N + (1 << 20)
     assert n < 2 * 2 * N * V // 50          # > 50x below the two logit tensors
     s2 = rg.make_shape(1, 8, 20000, 4096, 128256, chunk_rows=4096)
     assert rg.grpo_workspace_bytes(s2) < n and rg.grpo_chunk_rows(s2) == 4096
