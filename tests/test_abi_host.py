@@ -153,6 +153,38 @@ def test_validation_codes_without_a_device(lib):
               None) == 2
 
 
+def test_validation_codes_of_the_added_entry_points_without_a_device(lib):
+    """The shard and 8-bit backward entry points reject bad arguments before any launch."""
+    import rl_fine_tuning_gb300 as rg
+    P = 1 << 20
+    s = rg.make_shape(1, 4, 64, 128, 1024)
+    need = rg.grpo_workspace_bytes(s)
+    one = ctypes.c_float(1.0)
+    sh = lib.grpo_loss_fwd_bwd_shard
+    assert sh(P, P, P, P, P, P, ctypes.byref(s), None, one, P, need, P, P, P, P, None, P, None) == 1   # no counts
+    assert sh(P, P, P, P, P, P, ctypes.byref(s), P + 2, one, P, need, P, P, P, P, None, P, None) == 1  # misaligned
+    assert sh(P, P, P, P, P, P, ctypes.byref(s), P, one, P, need - 1, P, P, P, P, None, P, None) == 3
+    assert lib.grpo_loss_fwd_shard(P, P, P, P, P, P, ctypes.byref(s), None, P, need, P, None, P, None) == 1
+    assert lib.grpo_shard_counts(P, ctypes.byref(s), None, None) == 1
+    bad = rg.make_shape(1, 4, 64, 100, 1024)
+    assert lib.grpo_shard_counts(P, ctypes.byref(bad), P, None) == 2
+    f8 = lib.grpo_loss_fwd_bwd_fp8
+    s8 = rg.make_shape(1, 4, 64, 128, 1024, rg.E4M3)
+    n8 = rg.grpo_workspace_bytes(s8)
+    assert n8 > need
+    args = lambda shape, ws, dH=P, dW=P, scale=one: (P, P, P, scale, one, one, P, P, P, ctypes.byref(shape), P, ws,  # noqa: E731
+                                                     P, dH, dW, None, P, None)
+    assert f8(*args(s, need)) == 5                                       # 16-bit shape
+    assert f8(*args(s8, n8 - 1)) == 3                                    # workspace of the 16-bit layout is short
+    assert f8(*args(s8, n8, dH=P + 16)) == 1                             # dH only 16-byte aligned
+    assert f8(*args(s8, n8, dW=None)) == 1
+    assert f8(*args(s8, n8, scale=ctypes.c_float(0.0))) == 2             # a scale must be positive
+    b8 = rg.make_shape(1, 4, 64, 192, 1024, rg.E5M2)
+    assert f8(*args(b8, rg.grpo_workspace_bytes(b8))) == 2               # d not a multiple of 128
+    big = rg.make_shape(1, 8, 4096, 128, 1024, rg.E4M3, chunk_rows=16384 + 128)
+    assert f8(*args(big, rg.grpo_workspace_bytes(big))) == 2             # chunks above the sort's 16384 rows
+
+
 def test_status_strings_and_version(lib):
     import rl_fine_tuning_gb300 as rg
     assert rg.grpo_status_string(0) == "ok"

@@ -1,8 +1,9 @@
 """The build with device-side index checks (libgrpo_checked.so): a check made
 to fail on purpose reports GRPO_ERR_BOUNDS, and the parity cases with every
 tail (ragged V and d, several chunks, scattered and empty masks, degenerate
-shapes, fp16, 8-bit inputs, the workspace-free forward) run through it with
-no check firing and the same results as the oracle."""
+shapes, fp16, 8-bit inputs forward and backward, data-parallel shards, the
+workspace-free forward) run through it with no check firing and the same
+results as the oracle."""
 import numpy as np
 import pytest
 
@@ -19,7 +20,7 @@ import rl_fine_tuning_gb300 as rg  # noqa: E402
 from rl_fine_tuning_gb300 import build  # noqa: E402
 from gpu_harness import DeviceWorkload  # noqa: E402
 from test_gpu_parity import assert_fwd_parity, assert_grad_parity  # noqa: E402
-from test_gpu_fp8 import run_fp8  # noqa: E402
+from test_gpu_fp8 import assert_fp8_grad_parity, run_fp8, run_fp8_bwd  # noqa: E402
 
 
 @pytest.fixture()
@@ -99,3 +100,35 @@ def test_workspace_free_forward_through_the_checks(checked):
     res = dw.results()
     assert res["status"] == 0
     assert_fwd_parity(res, oracle.expected(wl, mask=res["mask"], want_dH=False, want_dW=False))
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_backward_through_the_checks(checked, fmt):
+    # ragged V over several chunks, and many rows per token (the sorted keys of the dW epilogue)
+    for over, chunk_rows in ((dict(G=4, L=500, d=384, V=3000, len_lo=1, len_hi=500), 256),
+                             (dict(G=4, L=256, d=256, V=200, len_lo=64, len_hi=256), 128)):
+        cfg = synth.make_config("tiny", **over)
+        res, exp = run_fp8_bwd(synth.generate_fp8(cfg, seed=43, fmt=fmt), chunk_rows=chunk_rows)
+        assert res["status"] == 0
+        assert_fp8_grad_parity(res, exp)
+
+
+def test_shards_through_the_checks(checked):
+    cfg = synth.make_config("tiny", n_groups=2, G=4, L=300, d=320, V=777, len_lo=40, len_hi=300)
+    wl = synth.generate(cfg, seed=4)
+    whole = DeviceWorkload(wl, chunk_rows=256).fwd_bwd()
+    dws = [DeviceWorkload(s, chunk_rows=256) for s in synth.split_groups(wl, 2)]
+    counts = [torch.zeros(2, dtype=torch.int32, device="cuda") for _ in dws]
+    for d, c in zip(dws, counts):
+        rg.grpo_shard_counts(d.mask, d.shape, c)
+    total = counts[0] + counts[1]
+    for d in dws:
+        rg.grpo_loss_fwd_bwd_shard(d.h_pol, d.h_ref, d.W, d.tokens, d.mask, d.adv, d.shape, total, 1.0, d.ws, d.loss,
+                                   d.dH, d.dW, d.found_inf, d.row_stats, d.status)
+    torch.cuda.synchronize()
+    assert all(int(d.status.item()) == 0 for d in dws)
+    n = dws[0].cfg.N
+    for r, d in enumerate(dws):
+        assert torch.equal(d.dH.view(torch.int16), whole.dH[r * n:(r + 1) * n].view(torch.int16))
+    loss = sum(float(d.loss.item()) for d in dws)
+    assert abs(loss - float(whole.loss.item())) <= 1e-6 * abs(float(whole.loss.item()))

@@ -117,3 +117,23 @@ def test_global_counts_below_the_shards_own_are_reported():
     assert int(d.status.item()) == 2                 # GRPO_ERR_SHAPE
     _run_shard(d, c)
     assert int(d.status.item()) == 0
+
+
+def test_forward_only_shards_add_up_to_the_whole_batch():
+    cfg = synth.make_config("tiny", n_groups=4, G=4, L=96, d=128, V=1024, len_lo=1, len_hi=96, n_zero_seq=2,
+                            sigma_ref=0.3)
+    wl = synth.generate(cfg, seed=3)
+    for loss_mode in (0, 1):
+        whole = DeviceWorkload(wl, loss_mode=loss_mode).fwd()
+        dws = [DeviceWorkload(s, loss_mode=loss_mode) for s in synth.split_groups(wl, 2)]
+        total = sum(_counts(d) for d in dws)
+        for d in dws:
+            rg.grpo_loss_fwd_shard(d.h_pol, d.h_ref, d.W, d.tokens, d.mask, d.adv, d.shape, total, d.ws, d.loss,
+                                   d.row_stats, d.status)
+        torch.cuda.synchronize()
+        assert all(int(d.status.item()) == 0 for d in dws)
+        loss = sum(float(d.loss.item()) for d in dws)
+        assert abs(loss - float(whole.loss.item())) <= 1e-6 * abs(float(whole.loss.item())), loss_mode
+        n = dws[0].cfg.N
+        for r, d in enumerate(dws):
+            assert torch.equal(d.row_stats, whole.row_stats[r * n:(r + 1) * n])
