@@ -207,9 +207,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kind, chunk_rows):
-    """DRAM bytes per launch of `kind` from the committed ncu summary, if it was
-    taken on the current kernel source with chunks of the same height; else None."""
+def ncu_traffic(kind, chunk_rows, field="dram_bytes_per_launch_full_workload"):
+    """DRAM bytes per launch of `kind` from the committed ncu summary (the median of
+    its captures; field="spread" gives their range), if it was taken on the current
+    kernel source with chunks of the same height; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -222,7 +223,7 @@ def ncu_traffic(kind, chunk_rows):
     ent = d.get("kernels", {}).get(kind)
     if not ent:
         return None
-    return ent.get("dram_bytes_per_launch_full_workload")
+    return ent.get(field)
 
 
 def cfg_dict(cfg, extra=None):
@@ -571,7 +572,8 @@ def run_ours(args, ranks):
     roofline = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": sustained, "unit": "TFLOP/s",
                 "frac": achieved / sustained, "peak_kind": f"bf16 dense sustained, {pk_kind}",
                 "traffic": ncu_traffic(dom, rg.grpo_chunk_rows(shape)),
-                "traffic_per": "full chunk launch (ncu DRAM read+write bytes)",
+                "traffic_spread": ncu_traffic(dom, rg.grpo_chunk_rows(shape), "spread"),
+                "traffic_per": "full chunk launch (ncu DRAM read+write bytes, median of captures in separate processes)",
                 # per full chunk of R rows, like traffic: its algorithmic flops, and the kernel's
                 # time per R rows (empty chunk slots exit at once and add nothing)
                 "rows_per_launch": R, "launches_with_rows": n_chunks_work,
