@@ -647,12 +647,13 @@ def run_forward_modes(args, ranks):
         if mode == "bf16":
             wl = synth.generate(cfg, seed=0)
             mats = [torch.from_numpy(a.view(np.int16)).cuda().view(torch.bfloat16) for a in (wl.h_pol, wl.h_ref, wl.W)]
-            shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.BF16, beta=cfg.beta, eps=cfg.eps)
+            shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.BF16, beta=cfg.beta, eps=cfg.eps,
+                                  chunk_rows=args.chunk_rows)
         else:
             wl = synth.generate_fp8(cfg, seed=0, fmt=mode)
             mats = [torch.from_numpy(a).cuda() for a in (wl.h_pol, wl.h_ref, wl.W)]
             shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, rg.E4M3 if mode == "e4m3" else rg.E5M2,
-                                  beta=cfg.beta, eps=cfg.eps)
+                                  beta=cfg.beta, eps=cfg.eps, chunk_rows=args.chunk_rows)
         tokens, lengths, rewards = (torch.from_numpy(a).cuda() for a in (wl.tokens, wl.lengths, wl.rewards))
         adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
         mask = torch.empty(cfg.N, dtype=torch.uint8, device="cuda")

@@ -80,7 +80,8 @@ typedef struct CUstream_st* grpo_stream_t;   /* the same type as cudaStream_t */
  *                 multiple of 128 and capped at N.  0 picks the default: 38
  *                 tiles of 128 rows (4864) when its dH work divides evenly
  *                 over the 76 SM pairs (d/256 a multiple of 4, e.g. d = 4096
- *                 or 5120), else 76 tiles (9728).  grpo_chunk_rows tells.
+ *                 or 5120), else 76 tiles (9728); 76 tiles for 8-bit shapes.
+ *                 grpo_chunk_rows tells.
  *   loss_mode   : GRPO_TOKEN_MEAN -- mean of ell_t over all masked rows;
  *                 GRPO_SEQUENCE_MEAN -- mean over completions (with at least
  *                 one masked row) of each completion's mean over its rows
@@ -315,6 +316,7 @@ enum {
     GRPO_PROF_DLOGITS,
     GRPO_PROF_DH,
     GRPO_PROF_DW,
+    GRPO_PROF_F8_PREP,   /* the 8-bit backward's group bounds and token sort */
     GRPO_PROF_KINDS
 };
 int grpo_profile_enable(int on);

@@ -25,7 +25,7 @@ __all__ = [
 ]
 
 # kernel kinds of the diagnostics interface, in the order of the GRPO_PROF_* enum
-PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "dlogits", "dh", "dw")
+PROF_KINDS = ("advantages", "mask", "index", "fwd", "merge", "clear", "gather", "dlogits", "dh", "dw", "f8_prep")
 
 BF16, FP16, E4M3, E5M2 = 0, 1, 2, 3
 TOKEN_MEAN, SEQUENCE_MEAN = 0, 1

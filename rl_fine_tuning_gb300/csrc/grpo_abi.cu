@@ -154,6 +154,9 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 }
 
 int default_chunk_rows(const grpo_shape& s) {
+    // 8-bit shapes: 76 tiles, so that dW's 8-bit K loop (twice as fast per row as the
+    // 16-bit one) stays long against its fp32 read-modify-write epilogue
+    if (is_fp8(s.dtype)) return kChunkTilesLarge * kBM;
     const int n_dt = (s.d + kBN - 1) / kBN;
     const int pairs_small = (kChunkTilesSmall + 1) / 2;
     const int tiles = (pairs_small * n_dt) % kChunkPairs == 0 ? kChunkTilesSmall : kChunkTilesLarge;
@@ -238,14 +241,15 @@ bool ws_layout(const grpo_shape& s, WsLayout* o) {
     o->mx = take(static_cast<size_t>(o->R) * o->nc32 * 4);
     o->ds = take(static_cast<size_t>(o->R) * o->V_pad * 2);
     o->hct = take(static_cast<size_t>(o->R) * s.d * 2);
-    o->rmax = o->qa = o->qb = o->gmax = o->keys = 0;
+    o->rmax = o->qa = o->qb = o->gmax = o->keys = o->tokpos = 0;
     if (is_fp8(s.dtype)) {
         // the 8-bit backward's buffers (its forward-only entry point needs none of them)
         o->rmax = take(static_cast<size_t>(N) * 4);
         o->qa = take(static_cast<size_t>(o->R) * o->V_pad);
         o->qb = take(static_cast<size_t>(o->R) * o->V_pad);
         o->gmax = take(static_cast<size_t>(o->nc32) * 4);
-        o->keys = take(static_cast<size_t>(o->R) * 8);
+        o->keys = take(static_cast<size_t>(o->n_sched - 2) * o->R * 8);   // every chunk's keys
+        o->tokpos = take(static_cast<size_t>(s.V) * 4);
     }
     o->total = off;
     return true;
@@ -505,6 +509,7 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
     cp.rmax = nullptr;
     cp.gmax = nullptr;
     cp.keys = nullptr;
+    cp.tokpos = nullptr;
     cp.hq = nullptr;
     cp.wq = nullptr;
     cp.scale_h = cp.scale_w = 1.f;
@@ -515,6 +520,7 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         cp.rmax = reinterpret_cast<const float*>(w + L.rmax);
         cp.gmax = reinterpret_cast<float*>(w + L.gmax);
         cp.keys = reinterpret_cast<unsigned long long*>(w + L.keys);
+        cp.tokpos = reinterpret_cast<int*>(w + L.tokpos);
         cp.hq = reinterpret_cast<const uint8_t*>(hc);
         cp.wq = static_cast<const uint8_t*>(in.W);
         cp.scale_h = f8->h_pol;
@@ -522,9 +528,16 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         cp.e5m2 = f8->e5m2 ? 1 : 0;
     }
     const int64_t max_chunks = (L.N + L.R - 1) / L.R;
+    // 8-bit backward: every chunk's (token, slot) keys sorted at once, one block per chunk
+    if (f8 && bwd && launch(GRPO_PROF_F8_PREP, st, [&] {
+            return launch_sort_keys(cp, static_cast<int>(max_chunks), st);
+        }) != cudaSuccess)
+        return GRPO_ERR_LAUNCH;
+    unsigned long long* keys_all = cp.keys;
     for (int64_t c = 0; c < max_chunks; ++c) {
         const int ci = static_cast<int>(c);
         cp.chunk = ci;
+        if (keys_all) cp.keys = keys_all + c * L.R;
         fp.chunk = ci;
         fp.sched = reinterpret_cast<int*>(w + L.sched) + 1 + ci;
         MergeParams mp = merge_params(in, L, w, ci, reinterpret_cast<const float4*>(w + L.partc), L.Sc);
@@ -545,11 +558,10 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         if (launch(GRPO_PROF_MERGE, st, [&] { return launch_merge(mp, st); }) != cudaSuccess) return GRPO_ERR_LAUNCH;
         if (!bwd) continue;
         if (f8) {
-            if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_f8_group_max(cp, dev.sm_count, st); }) !=
+            if (launch(GRPO_PROF_F8_PREP, st, [&] { return launch_f8_group_max(cp, dev.sm_count, st); }) !=
                     cudaSuccess ||
                 launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform_f8(cp, dev.sm_count, st); }) !=
                     cudaSuccess ||
-                launch(GRPO_PROF_DLOGITS, st, [&] { return launch_sort_keys(cp, st); }) != cudaSuccess ||
                 launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair_fp8(cp, mDS_k, mW_mn, dev.sm_count, st); }) !=
                     cudaSuccess ||
                 launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair_fp8(cp, mDS_mn, mHc_mn, dev.sm_count, st); }) !=

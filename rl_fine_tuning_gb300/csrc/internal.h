@@ -75,8 +75,9 @@ struct WsLayout {
     size_t counts, sched, seqcnt, tiles, rows, part, zt, lse, gco, ell, blocksum, hc, hcr, partc, mx, ds, total;
     // 8-bit inputs only (grpo_loss_fwd_bwd_fp8): row maxima [N] f32, the two code
     // buffers of the softmax part of the dlogits [R x V_pad] u8 each, the group
-    // scales [nc32] f32 and the sorted (token, slot) keys [R] u64
-    size_t rmax, qa, qb, gmax, keys;
+    // scales [nc32] f32, every chunk's sorted (token, slot) keys [max chunks x R]
+    // u64 and the first key of each token in the current chunk [V] i32
+    size_t rmax, qa, qb, gmax, keys, tokpos;
     size_t hct;      // the chunk's compact h_pol rows transposed, [d x R] 16-bit (dW's K-major B operand)
     int S, nps;      // forward-only path: vocabulary splits, N-tiles per split (partials by row)
     int Sc, npsc;    // chunked path: vocabulary splits, N-tiles per split (partials by chunk slot)
@@ -140,7 +141,9 @@ struct ChunkParams {
     uint8_t* qb;            // [R x V_pad]  P * 448 / gmax[group]
     const float* rmax;      // [N] row maximum of the policy logits
     float* gmax;            // [nc32] max over the chunk's rows of |P| bounds per 32-column group
-    unsigned long long* keys;   // [R] (token << 32 | slot) of the chunk's rows, ascending
+    unsigned long long* keys;   // (token << 32 | slot) of the chunk's rows, ascending: [R] of this chunk
+                                //   (the sort writes every chunk's, [max chunks x R], from the first chunk's base)
+    int* tokpos;            // [V] index in keys of the token's first key, -1 if no row of the chunk has it
     const uint8_t* hq;      // compact 8-bit h_pol rows of the chunk [R x d]
     const uint8_t* wq;      // 8-bit W [V x d]
     float scale_h, scale_w; // per-tensor scales of the 8-bit h_pol and W
@@ -200,7 +203,7 @@ cudaError_t launch_zero_masked_rows(const uint8_t* mask, int64_t N, int d, void*
 // 8-bit backward: group bounds, dlogit codes, sorted token keys, and the two GEMMs
 cudaError_t launch_f8_group_max(const ChunkParams& p, int sm_count, cudaStream_t st);
 cudaError_t launch_transform_f8(const ChunkParams& p, int sm_count, cudaStream_t st);
-cudaError_t launch_sort_keys(const ChunkParams& p, cudaStream_t st);
+cudaError_t launch_sort_keys(const ChunkParams& p, int max_chunks, cudaStream_t st);
 
 cudaError_t launch_wait_selftest(int* status, unsigned long long* waited_ns, cudaStream_t st);
 #ifdef GRPO_DEVICE_CHECKS

@@ -725,32 +725,53 @@ cudaError_t launch_transform(const ChunkParams& p, bool bf16, int R, int sm_coun
 
 // gmax[grp] = max over the chunk's rows of |g| exp(m_grp - lse): one bound of
 // |P| per 32-column group, shared by all rows of the chunk (zeroed
-// beforehand; non-negative floats order like their bit patterns).
-constexpr int kF8GroupRows = 64;
+// beforehand; non-negative floats order like their bit patterns).  A block
+// takes kF8GroupRows rows and keeps max_t (m_grp + log|g_t| - lse_t) per group,
+// so it needs one exponential per group; rows with g = 0 add nothing.
+constexpr int kF8GroupRows = 16;
 
 __global__ void __launch_bounds__(256) k_f8_group_max(const ChunkParams p) {
+    __shared__ float c_row[kF8GroupRows];
     if (p.chunk >= p.counts[C_NCHUNKS]) return;
     const int rc = p.counts[C_CHUNK_ROWS];
     const int c0 = p.chunk * rc;
     const int n_c = min(rc, p.counts[C_NVALID] - c0);
     const int s0 = blockIdx.x * kF8GroupRows;
     if (s0 >= n_c) return;
-    const int s1 = min(n_c, s0 + kF8GroupRows);
-    const int ng = (p.V + 31) / 32;
-    for (int grp = threadIdx.x; grp < ng; grp += blockDim.x) {
-        float m = 0.f;
-        for (int slot = s0; slot < s1; ++slot) {
+    const int nr = min(n_c - s0, kF8GroupRows);
+    if (threadIdx.x < kF8GroupRows) {
+        float c = -INFINITY;
+        const int slot = s0 + threadIdx.x;
+        if (static_cast<int>(threadIdx.x) < nr) {
             const int t = p.rows[c0 + slot];
-            if (!GRPO_DCHECK(t >= 0 && t < p.N && slot < p.R, p.status)) continue;
-            const float b = fabsf(p.gco[t]) * expf(p.mx[static_cast<int64_t>(slot) * p.nc32 + grp] - p.lse[t]);
-            m = fmaxf(m, b);
+            if (GRPO_DCHECK(t >= 0 && t < p.N && slot < p.R, p.status)) {
+                const float g = fabsf(p.gco[t]);
+                c = g > 0.f ? logf(g) - p.lse[t] : -INFINITY;
+            }
+            // tokpos[tok] = index of the token's first key in the chunk's sorted keys
+            const uint32_t tok = static_cast<uint32_t>(p.keys[slot] >> 32);
+            if ((slot == 0 || static_cast<uint32_t>(p.keys[slot - 1] >> 32) != tok) && tok < static_cast<uint32_t>(p.V))
+                p.tokpos[tok] = slot;
         }
-        atomicMax(reinterpret_cast<int*>(p.gmax) + grp, __float_as_int(m));
+        c_row[threadIdx.x] = c;
+    }
+    __syncthreads();
+    const int ng = (p.V + 31) / 32;
+    const float* mx0 = p.mx + static_cast<int64_t>(s0) * p.nc32;
+    for (int grp = threadIdx.x; grp < ng; grp += blockDim.x) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kF8GroupRows; ++r)
+            if (r < nr) m = fmaxf(m, mx0[static_cast<int64_t>(r) * p.nc32 + grp] + c_row[r]);
+        const float b = expf(m);   // 0 when every row of the block has g = 0
+        atomicMax(reinterpret_cast<int*>(p.gmax) + grp, __float_as_int(b));
     }
 }
 
 cudaError_t launch_f8_group_max(const ChunkParams& p, int sm_count, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(p.gmax, 0, static_cast<size_t>(p.nc32) * sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p.tokpos, 0xFF, static_cast<size_t>(p.V) * sizeof(int), st);
     if (e != cudaSuccess) return e;
     int blocks = (p.R + kF8GroupRows - 1) / kF8GroupRows;
     if (blocks < 1) blocks = 1;
@@ -777,16 +798,18 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkP
     const int c0 = p.chunk * rc;
     const int n_c = min(rc, p.counts[C_NVALID] - c0);
     const int n_fill = min(p.R, (n_c + kBM - 1) / kBM * kBM);
-    const int nvec = p.V_pad / 8;   // 8 columns per step: 16 bytes of exponentials, 8 bytes of each code
+    // one 32-column group per thread and step (its two scale factors are the group's):
+    // 64 bytes of exponentials in, 32 bytes of each code out
+    const int ngrp = p.V_pad / 32;
     const bool e5 = p.e5m2 != 0;
     for (int slot = blockIdx.x; slot < n_fill; slot += gridDim.x) {
         const uint4* erow = reinterpret_cast<const uint4*>(p.dS + static_cast<int64_t>(slot) * p.V_pad);
-        uint2* arow = reinterpret_cast<uint2*>(p.qa + static_cast<int64_t>(slot) * p.V_pad);
-        uint2* brow = reinterpret_cast<uint2*>(p.qb + static_cast<int64_t>(slot) * p.V_pad);
+        uint4* arow = reinterpret_cast<uint4*>(p.qa + static_cast<int64_t>(slot) * p.V_pad);
+        uint4* brow = reinterpret_cast<uint4*>(p.qb + static_cast<int64_t>(slot) * p.V_pad);
         if (slot >= n_c) {
-            for (int i = threadIdx.x; i < nvec; i += kTransformThreads) {
-                arow[i] = make_uint2(0, 0);
-                brow[i] = make_uint2(0, 0);
+            for (int i = threadIdx.x; i < 2 * ngrp; i += kTransformThreads) {
+                arow[i] = make_uint4(0, 0, 0, 0);
+                brow[i] = make_uint4(0, 0, 0, 0);
             }
             continue;
         }
@@ -797,30 +820,42 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkP
         const float zmax = p.rmax[t];
         const float sa = g == 0.f ? 0.f : copysignf(448.f, g);
         const float* mrow = p.mx + static_cast<int64_t>(slot) * p.nc32;
-        for (int i = threadIdx.x; i < nvec; i += kTransformThreads) {
-            const int v0 = i * 8;
-            const int grp = v0 >> 5;
-            float ca = 0.f, cb = 0.f;
-            if (v0 < p.V) {
-                const float m = mrow[grp];
-                ca = sa * expf(m - zmax);
-                const float gm = p.gmax[grp];
-                cb = gm > 0.f ? g * expf(m - lse) * (448.f / gm) : 0.f;
-            }
-            const uint4 u = erow[i];
-            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-            uint32_t oa[4], ob[4];
+        for (int grp = threadIdx.x; grp < ngrp; grp += kTransformThreads) {
+            const int v0 = grp * 32;
+            uint32_t oa[8], ob[8];
+            if (v0 >= p.V) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float e0 = __uint_as_float(w[j] << 16);
-                float e1 = __uint_as_float(w[j] & 0xFFFF0000u);
-                if (v0 + 2 * j >= p.V) e0 = 0.f;
-                if (v0 + 2 * j + 1 >= p.V) e1 = 0.f;
-                oa[j] = f8x2(ca * e0, ca * e1, e5);
-                ob[j] = f8x2(cb * e0, cb * e1, e5);
+                for (int j = 0; j < 8; ++j) oa[j] = ob[j] = 0u;
+            } else {
+                const float m = mrow[grp];
+                const float ca = sa * expf(m - zmax);
+                const float gm = p.gmax[grp];
+                const float cb = gm > 0.f ? g * expf(m - lse) * (448.f / gm) : 0.f;
+                uint4 u[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) u[j] = erow[4 * grp + j];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+                    uint32_t pa[4], pb[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int v = v0 + 8 * j + 2 * k;
+                        const float e0 = v < p.V ? __uint_as_float(w[k] << 16) : 0.f;
+                        const float e1 = v + 1 < p.V ? __uint_as_float(w[k] & 0xFFFF0000u) : 0.f;
+                        pa[k] = f8x2(ca * e0, ca * e1, e5);
+                        pb[k] = f8x2(cb * e0, cb * e1, e5);
+                    }
+                    oa[2 * j] = pa[0] | (pa[1] << 16);
+                    oa[2 * j + 1] = pa[2] | (pa[3] << 16);
+                    ob[2 * j] = pb[0] | (pb[1] << 16);
+                    ob[2 * j + 1] = pb[2] | (pb[3] << 16);
+                }
             }
-            arow[i] = make_uint2(oa[0] | (oa[1] << 16), oa[2] | (oa[3] << 16));
-            brow[i] = make_uint2(ob[0] | (ob[1] << 16), ob[2] | (ob[3] << 16));
+            arow[2 * grp] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+            arow[2 * grp + 1] = make_uint4(oa[4], oa[5], oa[6], oa[7]);
+            brow[2 * grp] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+            brow[2 * grp + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
         }
     }
 }
@@ -832,14 +867,16 @@ cudaError_t launch_transform_f8(const ChunkParams& p, int sm_count, cudaStream_t
     return cudaGetLastError();
 }
 
-// The chunk's (token << 32 | slot) keys in ascending order, by a bitonic sort
-// of the next power of two >= R keys in one block's shared memory (padding
-// keys sort last).  The dW epilogue finds the rows of a vocabulary row in it.
+// Every chunk's (token << 32 | slot) keys in ascending order, one block per
+// chunk, by a bitonic sort of the next power of two >= R keys in the block's
+// shared memory (padding keys sort last).  Chunk c's keys go to keys[c * R ..].
+// The dW epilogue finds the rows of a vocabulary row among them.
 __global__ void __launch_bounds__(1024) k_sort_keys(const ChunkParams p, int n_pow2) {
     extern __shared__ unsigned long long keys_sh[];
-    if (p.chunk >= p.counts[C_NCHUNKS]) return;
+    const int chunk = blockIdx.x;
+    if (chunk >= p.counts[C_NCHUNKS]) return;
     const int rc = p.counts[C_CHUNK_ROWS];
-    const int c0 = p.chunk * rc;
+    const int c0 = chunk * rc;
     const int n_c = min(rc, p.counts[C_NVALID] - c0);
     for (int i = threadIdx.x; i < n_pow2; i += blockDim.x) {
         unsigned long long k = ~0ull;
@@ -867,10 +904,11 @@ __global__ void __launch_bounds__(1024) k_sort_keys(const ChunkParams p, int n_p
             __syncthreads();
         }
     }
-    for (int i = threadIdx.x; i < n_c && i < p.R; i += blockDim.x) p.keys[i] = keys_sh[i];
+    unsigned long long* out = p.keys + static_cast<int64_t>(chunk) * p.R;
+    for (int i = threadIdx.x; i < n_c && i < p.R; i += blockDim.x) out[i] = keys_sh[i];
 }
 
-cudaError_t launch_sort_keys(const ChunkParams& p, cudaStream_t st) {
+cudaError_t launch_sort_keys(const ChunkParams& p, int max_chunks, cudaStream_t st) {
     int n_pow2 = 1;
     while (n_pow2 < p.R) n_pow2 <<= 1;
     if (n_pow2 > kF8SortMax) return cudaErrorInvalidValue;
@@ -878,7 +916,7 @@ cudaError_t launch_sort_keys(const ChunkParams& p, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(k_sort_keys, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    k_sort_keys<<<1, 1024, smem, st>>>(p, n_pow2);
+    k_sort_keys<<<max_chunks > 0 ? max_chunks : 1, 1024, smem, st>>>(p, n_pow2);
     return cudaGetLastError();
 }
 

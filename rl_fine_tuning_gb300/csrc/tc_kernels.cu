@@ -1008,16 +1008,10 @@ struct DwPairF8T : DwPairT {
         const bool valid = v < p.V;
         if (!__any_sync(0xffffffffu, valid)) return;
         const bool first_chunk = p.chunk == 0;
-        // the chunk's rows whose sampled token is v: a run of the sorted keys
-        int lo = 0, hi = sc.n_c;
-        const unsigned long long key = static_cast<unsigned long long>(static_cast<uint32_t>(valid ? v : 0)) << 32;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (p.keys[mid] < key) lo = mid + 1;
-            else hi = mid;
-        }
+        // the chunk's rows whose sampled token is v: a run of the sorted keys from tokpos[v]
+        const int lo = valid ? p.tokpos[v] : -1;
         int n_hit = 0;
-        while (valid && lo + n_hit < sc.n_c && (p.keys[lo + n_hit] >> 32) == static_cast<unsigned long long>(v))
+        while (lo >= 0 && lo + n_hit < sc.n_c && (p.keys[lo + n_hit] >> 32) == static_cast<unsigned long long>(v))
             ++n_hit;
         const float fb = valid ? p.gmax[v >> 5] * (1.f / 448.f) : 0.f;
         const float f = sc.winv * p.scale_h;
@@ -1043,17 +1037,24 @@ struct DwPairF8T : DwPairT {
                 for (int j = 0; j < 32; ++j) oh[j] = fmaf(g, hv[j], oh[j]);
             }
             float* o = out + col0;
+            // the four loads of the block first (they are in flight together), then the stores
+            float prev[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) prev[j] = 0.f;
+            if (!first_chunk) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float q[8];
+                    ld_global_v8(o + 8 * j, q);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) prev[8 * j + i] = q[i];
+                }
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 float r[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) r[i] = f * (oh[8 * j + i] - fb * x[8 * j + i]);
-                if (!first_chunk) {
-                    float prev[8];
-                    ld_global_v8(o + 8 * j, prev);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) r[i] += prev[i];
-                }
+                for (int i = 0; i < 8; ++i) r[i] = f * (oh[8 * j + i] - fb * x[8 * j + i]) + prev[8 * j + i];
                 st_global_v8(o + 8 * j, __float_as_uint(r[0]), __float_as_uint(r[1]), __float_as_uint(r[2]),
                              __float_as_uint(r[3]), __float_as_uint(r[4]), __float_as_uint(r[5]),
                              __float_as_uint(r[6]), __float_as_uint(r[7]));

@@ -108,10 +108,16 @@ def test_shape_defaults_and_workspace_bytes(lib):
     assert rg.grpo_chunk_rows(rg.make_shape(1, 4, 64, 128, 1024)) == 256            # capped at N
     assert rg.grpo_chunk_rows(rg.make_shape(1, 8, 20000, 100, 128256)) == 0         # invalid shape
     V_pad, nc32 = (V + 63) // 64 * 64, ((V + 31) // 32 + 7) // 8 * 8
+    R8 = 76 * 128                            # 8-bit shapes default to 76-tile chunks
+    n76 = rg.grpo_workspace_bytes(rg.make_shape(1, 8, 20000, 4096, 128256, chunk_rows=R8))
     for fp8 in (rg.E4M3, rg.E5M2):          # the 16-bit layout plus the 8-bit backward's buffers
-        n8 = rg.grpo_workspace_bytes(rg.make_shape(1, 8, 20000, 4096, 128256, fp8))
-        extra = 2 * R * V_pad + 4 * N + 4 * nc32 + 8 * R     # two code buffers, row maxima, group scales, keys
-        assert n + extra <= n8 <= n + extra + 5 * 256
+        s8 = rg.make_shape(1, 8, 20000, 4096, 128256, fp8)
+        assert rg.grpo_chunk_rows(s8) == R8
+        n8 = rg.grpo_workspace_bytes(s8)
+        # two code buffers, row maxima, group scales, keys, first key of each token
+        max_chunks = (N + R8 - 1) // R8
+        extra = 2 * R8 * V_pad + 4 * N + 4 * nc32 + 8 * max_chunks * R8 + 4 * V
+        assert n76 + extra <= n8 <= n76 + extra + 6 * 256
     for bad in (dict(d=100), dict(d=0), dict(V=0), dict(G=0), dict(L=0)):
         b = rg.make_shape(1, 8, 20000, 4096, 128256)
         for k, v in bad.items():
