@@ -3,9 +3,13 @@
  * no torch): device memory from cudaMalloc, inputs made on the host from a
  * small linear congruential generator and copied over, then
  * grpo_group_advantages, grpo_build_mask, grpo_loss_fwd and
- * grpo_loss_fwd_bwd on one stream.  Prints "ok <loss> <checksum>" and exits 0
+ * grpo_loss_fwd_bwd on one stream.  Then the same batch as two data-parallel
+ * shards of one prompt group each (grpo_shard_counts, the counts summed on the
+ * host, grpo_loss_fwd_bwd_shard).  Prints "ok <loss> <checksum>" and exits 0
  * when every call returns 0, the device status words read 0, the losses of
- * the two entry points are equal bit for bit and every gradient is finite.
+ * the two entry points are equal bit for bit, every gradient is finite, the
+ * shards' dH rows equal the batch's bit for bit, and their loss shares and dW
+ * add up to the batch's.
  */
 #include <math.h>
 #include <stdint.h>
@@ -141,6 +145,85 @@ int main(void) {
     if (memcmp(&loss, &loss2, 4) != 0) {
         fprintf(stderr, "losses differ: %.9g vs %.9g\n", loss, loss2);
         return 1;
+    }
+    /* the batch as two shards of one prompt group each (rows [r*N/2, (r+1)*N/2)) */
+    {
+        grpo_shape sh;
+        grpo_shape_init(&sh, 1, G, L, d, V, GRPO_BF16);
+        sh.chunk_rows = 256;
+        const int Ns = G * L;
+        const size_t ws_s = grpo_workspace_bytes(&sh);
+        void *s_ws, *s_cnt[2], *s_gcnt, *s_loss[2], *s_dH[2], *s_dW[2], *s_fi;
+        CUDA(cudaMalloc(&s_ws, ws_s));
+        CUDA(cudaMalloc(&s_gcnt, 8));
+        CUDA(cudaMalloc(&s_fi, 4));
+        int32_t cnt[2][2], total[2] = {0, 0};
+        for (int r = 0; r < 2; ++r) {
+            CUDA(cudaMalloc(&s_cnt[r], 8));
+            CUDA(cudaMalloc(&s_loss[r], 4));
+            CUDA(cudaMalloc(&s_dH[r], (size_t)Ns * d * 2));
+            CUDA(cudaMalloc(&s_dW[r], (size_t)V * d * 4));
+            CK(grpo_shard_counts((const uint8_t*)d_mask + (size_t)r * Ns, &sh, s_cnt[r], gs));
+        }
+        CUDA(cudaStreamSynchronize(st));
+        for (int r = 0; r < 2; ++r) {
+            CUDA(cudaMemcpy(cnt[r], s_cnt[r], 8, cudaMemcpyDeviceToHost));
+            total[0] += cnt[r][0];
+            total[1] += cnt[r][1];
+        }
+        CUDA(cudaMemcpy(s_gcnt, total, 8, cudaMemcpyHostToDevice));   /* the host does the "all-reduce" */
+        float share[2];
+        for (int r = 0; r < 2; ++r) {
+            const size_t ro = (size_t)r * Ns;
+            CK(grpo_loss_fwd_bwd_shard((const char*)d_hp + ro * d * 2, (const char*)d_hr + ro * d * 2, d_W,
+                                       (const int32_t*)d_tok + ro, (const uint8_t*)d_mask + ro,
+                                       (const float*)d_adv + (size_t)r * G, &sh, s_gcnt, 1.0f, s_ws, ws_s, s_loss[r],
+                                       s_dH[r], s_dW[r], s_fi, NULL, d_status, gs));
+            CUDA(cudaStreamSynchronize(st));
+            CUDA(cudaMemcpy(&status, d_status, 4, cudaMemcpyDeviceToHost));
+            CUDA(cudaMemcpy(&share[r], s_loss[r], 4, cudaMemcpyDeviceToHost));
+            if (status != 0) {
+                fprintf(stderr, "shard %d device status %d\n", r, status);
+                return 1;
+            }
+        }
+        if (fabs((double)share[0] + share[1] - loss2) > 1e-6 * fabs(loss2)) {
+            fprintf(stderr, "shard losses %.9g + %.9g != %.9g\n", share[0], share[1], loss2);
+            return 1;
+        }
+        uint16_t* sdH = malloc((size_t)Ns * d * 2);
+        float* sdW0 = malloc((size_t)V * d * 4);
+        float* sdW1 = malloc((size_t)V * d * 4);
+        for (int r = 0; r < 2; ++r) {
+            CUDA(cudaMemcpy(sdH, s_dH[r], (size_t)Ns * d * 2, cudaMemcpyDeviceToHost));
+            if (memcmp(sdH, dH_host + (size_t)r * Ns * d, (size_t)Ns * d * 2) != 0) {
+                fprintf(stderr, "shard %d dH rows differ from the batch's\n", r);
+                return 1;
+            }
+        }
+        CUDA(cudaMemcpy(sdW0, s_dW[0], (size_t)V * d * 4, cudaMemcpyDeviceToHost));
+        CUDA(cudaMemcpy(sdW1, s_dW[1], (size_t)V * d * 4, cudaMemcpyDeviceToHost));
+        double top = 0.0, worst = 0.0;
+        for (int64_t i = 0; i < (int64_t)V * d; ++i) {
+            top = fmax(top, fabs(dW_host[i]));
+            worst = fmax(worst, fabs((double)sdW0[i] + sdW1[i] - dW_host[i]));
+        }
+        if (!(worst <= 1e-5 * top)) {
+            fprintf(stderr, "shard dW sum differs by %.3g (max %.3g)\n", worst, top);
+            return 1;
+        }
+        free(sdH);
+        free(sdW0);
+        free(sdW1);
+        for (int r = 0; r < 2; ++r) {
+            cudaFree(s_cnt[r]);
+            cudaFree(s_loss[r]);
+            cudaFree(s_dH[r]);
+            cudaFree(s_dW[r]);
+        }
+        cudaFree(s_ws);
+        cudaFree(s_gcnt);
+        cudaFree(s_fi);
     }
     double checksum = 0.0;
     for (int64_t i = 0; i < (int64_t)N * d; ++i) {

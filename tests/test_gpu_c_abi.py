@@ -1,8 +1,9 @@
 """The C ABI from plain C: a program that includes only grpo.h and the CUDA
 runtime header, links libgrpo.so and runs a whole step (advantages, mask,
-forward, forward+backward) on its own cudaMalloc'd buffers; it checks its own
-statuses and the bitwise equality of the two losses, and two runs print the
-same bits."""
+forward, forward+backward) on its own cudaMalloc'd buffers, then the same
+batch as two data-parallel shards; it checks its own statuses, the bitwise
+equality of the two losses, and that the shards add up to the batch; two runs
+print the same bits."""
 import os
 import shutil
 import subprocess
