@@ -283,7 +283,7 @@ int grpo_loss_fwd_bwd_fp8(const void* h_pol, const void* h_ref, const void* W, f
  *   GRPO_ERR_WORKSPACE before anything is launched.
  *   The first call on a device looks up the array's device address (a
  *   synchronous runtime call).  Under lazy module loading (the CUDA default)
- *   that first call is also when the driver loads this library's device code
+ *   that first call is also when the CUDA driver loads this library's device code
  *   and places the array in device memory, so make it before the device's
  *   free memory is handed to anything else (an inference engine's pool), and
  *   before any stream capture; later calls need no new memory.
