@@ -96,12 +96,12 @@ def test_fp8_forward_full_size_sampled_rows(fmt):
     assert abs(res["loss"] - ell.mean()) <= 1e-5 * max(1e-3, abs(ell.mean()))
 
 
-def run_fp8_bwd(wl8, mask=None, chunk_rows=0, want_expected=True):
+def run_fp8_bwd(wl8, mask=None, chunk_rows=0, want_expected=True, objective=0, loss_mode=0):
     cfg = wl8.cfg
     s_pol, s_ref, s_w = wl8.extra["scales"]
     dtype = rg.E5M2 if wl8.extra.get("fp8") == "e5m2" else rg.E4M3
     shape = rg.make_shape(cfg.n_groups, cfg.G, cfg.L, cfg.d, cfg.V, dtype, beta=cfg.beta, eps=cfg.eps,
-                          chunk_rows=chunk_rows)
+                          chunk_rows=chunk_rows, objective=objective, loss_mode=loss_mode)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()  # noqa: E731
     h_pol, h_ref, W = dev(wl8.h_pol), dev(wl8.h_ref), dev(wl8.W)
     tokens, lengths, rewards = dev(wl8.tokens), dev(wl8.lengths), dev(wl8.rewards)
@@ -125,7 +125,8 @@ def run_fp8_bwd(wl8, mask=None, chunk_rows=0, want_expected=True):
     res = dict(loss=float(loss.item()), status=int(status.item()), row_stats=stats.cpu().numpy().astype(np.float64),
                adv=adv.cpu().numpy(), mask=m.cpu().numpy(), dH=dH.float().cpu().numpy().astype(np.float64),
                dW=dW.cpu().numpy().astype(np.float64))
-    exp = oracle.expected(oracle.dequantized_workload(wl8), mask=res["mask"]) if want_expected else None
+    exp = (oracle.expected(oracle.dequantized_workload(wl8), mask=res["mask"], objective=objective,
+                           loss_mode=loss_mode) if want_expected else None)
     return res, exp
 
 
@@ -223,3 +224,13 @@ def test_fp8_backward_bad_token_and_reproducibility():
     res, _ = run_fp8_bwd(wl8, chunk_rows=256, want_expected=False)
     assert res["status"] == 2
     assert np.all(np.isfinite(res["dH"])) and np.all(np.isfinite(res["dW"]))
+
+
+@pytest.mark.parametrize("objective", ["no_detach", "reverse_kl_q", "forward_kl"])
+def test_fp8_backward_objective_variants_and_sequence_mean(objective):
+    # three prompt groups, a fully masked completion, a KL large enough to matter, per-completion mean
+    cfg = synth.make_config("tiny", n_groups=3, G=4, L=150, d=256, V=1000, len_lo=1, len_hi=150, n_zero_seq=1,
+                            sigma_ref=0.3)
+    res, exp = run_fp8_bwd(synth.generate_fp8(cfg, seed=48, fmt="e4m3"), chunk_rows=256, objective=objective,
+                           loss_mode=1)
+    assert_fp8_grad_parity(res, exp)
