@@ -528,6 +528,10 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         cp.e5m2 = f8->e5m2 ? 1 : 0;
     }
     const int64_t max_chunks = (L.N + L.R - 1) / L.R;
+    // dH in 512-column units when a full chunk's units divide evenly over the SM pairs
+    const int dh_pairs_of_tiles = (L.R / kBM + 1) / 2;
+    const int dh_wide_tiles = (s.d + 2 * kBN - 1) / (2 * kBN);
+    const bool dh_wide = (dh_pairs_of_tiles * dh_wide_tiles) % (dev.sm_count / 2) == 0;
     // 8-bit backward: every chunk's (token, slot) keys sorted at once, one block per chunk
     if (f8 && bwd && launch(GRPO_PROF_F8_PREP, st, [&] {
             return launch_sort_keys(cp, static_cast<int>(max_chunks), st);
@@ -572,8 +576,9 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
         if (launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform(cp, bf16, L.R, dev.sm_count, st); }) !=
             cudaSuccess)
             return GRPO_ERR_LAUNCH;
-        if (launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, st); }) !=
-            cudaSuccess)
+        if (launch(GRPO_PROF_DH, st, [&] {
+                return launch_dh_pair(cp, mDS_k, mW_mn, dev.sm_count, bf16, dh_wide, st);
+            }) != cudaSuccess)
             return GRPO_ERR_LAUNCH;
         if (launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair(cp, mDS_mn, mHc_mn, dev.sm_count, bf16, st); }) !=
             cudaSuccess)

@@ -216,8 +216,9 @@ cudaError_t launch_fwd_pair(const FwdParams& p, const CUtensorMap& mHp, const CU
                             const CUtensorMap& mW, int n_sm, bool bf16, cudaStream_t st);
 cudaError_t launch_fwd_pair_fp8(const FwdParams& p, const CUtensorMap& mHp, const CUtensorMap& mHr,
                                 const CUtensorMap& mW, int n_sm, bool e5m2, cudaStream_t st);
+// wide: 512-column units (see DhPairWideT), for chunks whose wide units divide evenly over the SM pairs
 cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm,
-                           bool bf16, cudaStream_t st);
+                           bool bf16, bool wide, cudaStream_t st);
 cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
                            bool bf16, cudaStream_t st);
 cudaError_t launch_dh_pair_fp8(const ChunkParams& p, const CUtensorMap& mQa, const CUtensorMap& mWmn, int n_sm,

@@ -760,6 +760,108 @@ struct DhPairT {
     __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
 };
 
+// dH with 512-column units: one staged 128-row dlogits tile feeds two 256-wide
+// d tiles (two M=256 MMAs per K sub-step into the two halves of tensor
+// memory), so the dlogits are read half as often and W in half as many waves.
+// Used where its units still divide evenly over the SM pairs.
+struct DhPairWideT {
+    static constexpr int kStages = 4;
+    static constexpr int kStageBytes = 16384 + 2 * 16384;   // A (128 slots x 64 vocab), 2 x B half (64 vocab x 128 d)
+    static constexpr bool kWideAcc = true;
+    using Params = ChunkParams;
+    using Sched = ChunkSched;
+    struct Coord {
+        int m0, n0;
+    };
+    struct Epi {
+        int unused;
+    };
+    // unit -> (pair of 128-row tiles, 512-wide d tile); the CTA of rank r takes m-tile 2*pair + r
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!chunk_setup(p, sc, 2)) return false;
+        sc.n_nt = (p.d + 2 * kBN - 1) / (2 * kBN);
+        sc.n_g = (sc.n_mt + 1) / 2;
+        sc.ks = (p.V + kBK - 1) / kBK;
+        sc.n_units = sc.n_g * sc.n_nt;
+        return true;
+    }
+    __device__ static int mtile(const Sched& sc, int unit, int rank) { return (unit / sc.n_nt) * 2 + rank; }
+    __device__ static int dtile(const Sched& sc, int unit) { return unit % sc.n_nt; }
+    __device__ static int items(const Params&, const Sched&, int) { return 1; }
+    __device__ static int ksteps(const Params&, const Sched& sc, int) { return sc.ks; }
+    __device__ static Coord coord(const Params&, const Sched& sc, int unit, int, int rank) {
+        return Coord{mtile(sc, unit, rank) * kBM, dtile(sc, unit) * 2 * kBN};
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
+        uint32_t b = 2 * 16384;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (c.n0 + h * kBN + r * 128 + 64 * j < p.d) b += 8192;
+        return b;
+    }
+    __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(mA, bar, st, k * kBK, c.m0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = c.n0 + h * kBN + rank * 128 + 64 * j;
+                if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384 + 16384 * h + 8192 * j, col, k * kBK);
+            }
+    }
+    template <bool kBf16>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f16(256, 256, kBf16, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = desc_kmajor(st + kk * 32);
+            const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+            umma_pair_f16(acc, a, desc_mnmajor(st + 16384 + kk * 2048), idesc, accum);
+            umma_pair_f16(acc + 256, a, desc_mnmajor(st + 32768 + kk * 2048), idesc, accum);
+        }
+    }
+    __device__ static void epi_begin(const Params&, const Sched&, int, int, int, Epi&) {}
+    template <bool kBf16>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int slot = mtile(sc, unit, rank) * kBM + row;
+        const int n0 = dtile(sc, unit) * 2 * kBN;
+        bool valid = slot < sc.n_c;
+        if (!__any_sync(0xffffffffu, valid)) return;
+        const int t = valid ? p.rows[sc.c0 + slot] : 0;
+        if (valid && !GRPO_DCHECK(t >= 0 && t < p.N, p.status)) valid = false;
+        uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
+        bool bad = false;
+#pragma unroll 1
+        for (int c = 0; c < 2 * kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) pk[j / 2] = pack2(v[j] * sc.winv, v[j + 1] * sc.winv, kBf16);
+            if (!kBf16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) bad |= half2_nonfinite(pk[j]);
+            }
+            if (valid) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    st_global_v8(out + col0 + 16 * h, pk[8 * h], pk[8 * h + 1], pk[8 * h + 2], pk[8 * h + 3],
+                                 pk[8 * h + 4], pk[8 * h + 5], pk[8 * h + 6], pk[8 * h + 7]);
+            }
+        }
+        if (bad && valid) atomicOr(p.found_inf, 1);
+    }
+    __device__ static void epi_end(const Params&, const Sched&, int, Epi&) {}
+};
+
 struct DwPairT {
     static constexpr int kStages = 7;
     static constexpr int kStageBytes = 16384 + 16384;   // A (64 slots x 128 vocab), B half (128 d x 64 slots)
@@ -1070,6 +1172,29 @@ struct DwPairF8T5 : DwPairF8T {
     }
 };
 
+// Accumulators of the pair engine: by default two 256-column buffers in tensor
+// memory, used alternately so an epilogue overlaps the next item's MMAs; a
+// traits class with kWideAcc uses all 512 columns as one buffer (its items are
+// long enough that the epilogue's share is small).
+template <class T>
+struct WideAcc {
+    template <class U>
+    static constexpr bool get(decltype(U::kWideAcc)*) { return U::kWideAcc; }
+    template <class U>
+    static constexpr bool get(...) { return false; }
+    static constexpr bool value = get<T>(nullptr);
+};
+
+template <class T>
+__device__ __forceinline__ int acc_buf(int it) {
+    return WideAcc<T>::value ? 0 : (it & 1);
+}
+
+template <class T>
+__device__ __forceinline__ uint32_t acc_phase(int it) {
+    return WideAcc<T>::value ? (static_cast<uint32_t>(it) & 1u) : (static_cast<uint32_t>(it >> 1) & 1u);
+}
+
 template <class T, bool kBf16>
 __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const CUtensorMap& mA, const CUtensorMap& mA2,
                                              const CUtensorMap& mB) {
@@ -1155,8 +1280,8 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
                 const int n_items = T::items(p, sc, unit);
                 const int ks = T::ksteps(p, sc, unit);
                 for (int item = 0; item < n_items; ++item, ++it) {
-                    const int b = it & 1;
-                    const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+                    const int b = acc_buf<T>(it);
+                    const uint32_t aph = acc_phase<T>(it);
                     if (!mbar_wait(&sm.acc_empty[b], aph ^ 1u, sm.abort_flag, status)) goto mma_done;
                     tc_fence_after();
                     const uint32_t acc = tmem + b * 256;
@@ -1198,8 +1323,8 @@ __device__ __forceinline__ void tc_pair_body(const typename T::Params& p, const 
             typename T::Epi e;
             T::epi_begin(p, sc, unit, rank, row, e);
             for (int item = 0; item < n_items; ++item, ++it) {
-                const int b = it & 1;
-                const uint32_t aph = static_cast<uint32_t>(it >> 1) & 1u;
+                const int b = acc_buf<T>(it);
+                const uint32_t aph = acc_phase<T>(it);
                 if (!mbar_wait(&sm.acc_full[b], aph, sm.abort_flag, status)) goto epi_done;
                 tc_fence_after();
                 T::template epi_item<kBf16>(p, sc, unit, item, rank, tq + b * 256, e);
@@ -1303,6 +1428,7 @@ GRPO_PAIR_KERNEL(grpo_fwd_pair_kernel, FwdPairT)
 GRPO_PAIR_KERNEL(grpo_fwd_pair_e4m3_kernel, FwdPairF8T<false>)
 GRPO_PAIR_KERNEL(grpo_fwd_pair_e5m2_kernel, FwdPairF8T<true>)
 GRPO_PAIR_KERNEL(grpo_dh_pair_kernel, DhPairT)
+GRPO_PAIR_KERNEL(grpo_dh_pair_wide_kernel, DhPairWideT)
 GRPO_PAIR_KERNEL(grpo_dw_pair_kernel, DwPairT)
 GRPO_PAIR_KERNEL(grpo_dh_pair_e4m3_kernel, DhPairF8T)
 GRPO_PAIR_KERNEL(grpo_dh_pair_e5m2_kernel, DhPairF8T5)
@@ -1354,7 +1480,10 @@ cudaError_t launch_fwd_pair_fp8(const FwdParams& p, const CUtensorMap& mHp, cons
 }
 
 cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const CUtensorMap& mWmn, int n_sm, bool bf16,
-                           cudaStream_t st) {
+                           bool wide, cudaStream_t st) {
+    if (wide)
+        return bf16 ? launch_tc<DhPairWideT, 2>(grpo_dh_pair_wide_kernel<true>, p, mDS, mDS, mWmn, n_sm, st)
+                    : launch_tc<DhPairWideT, 2>(grpo_dh_pair_wide_kernel<false>, p, mDS, mDS, mWmn, n_sm, st);
     return bf16 ? launch_tc<DhPairT, 2>(grpo_dh_pair_kernel<true>, p, mDS, mDS, mWmn, n_sm, st)
                 : launch_tc<DhPairT, 2>(grpo_dh_pair_kernel<false>, p, mDS, mDS, mWmn, n_sm, st);
 }

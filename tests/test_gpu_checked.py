@@ -47,6 +47,7 @@ CASES = [
     ("d64", dict(d=64, V=200), 0, None),
     ("no_even_split", dict(G=2, L=100, d=64, V=257 * 256, len_lo=40, len_hi=100), 0, None),
     ("all_masked", dict(), 0, "empty"),
+    ("wide_dh", dict(G=4, L=4096, d=768, V=1000, len_lo=1500, len_hi=4096), 76 * 128, None),   # 512-column dH units
 ]
 
 

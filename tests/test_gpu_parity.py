@@ -152,6 +152,17 @@ def test_chunk_heights_with_odd_tile_counts(chunk_rows):
     assert_grad_parity(res, exp)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_wide_dh_units(dtype):
+    # 76-tile chunks with d = 768: 38 tile pairs x 2 wide d tiles of 512 columns divide over the 76 SM
+    # pairs, so dH runs in 512-column units, the second one half past d; two chunks, the second partial
+    cfg = synth.make_config("tiny", dtype=dtype, G=4, L=4096, d=768, V=1000, len_lo=1500, len_hi=4096)
+    _, dw, res, exp = _run(cfg, seed=31, chunk_rows=76 * 128, loss_scale=256.0 if dtype == "fp16" else 1.0)
+    assert exp["n_valid"] > 76 * 128
+    assert_fwd_parity(res, exp)
+    assert_grad_parity(res, exp, loss_scale=256.0 if dtype == "fp16" else 1.0)
+
+
 def test_fwd_bwd_scattered_mask():
     cfg = synth.make_config("tiny", G=2, L=200, d=128, V=777)
     rng = np.random.default_rng(5)
