@@ -758,12 +758,14 @@ static int validate_fp8(const Inputs& in8, float scale_h_pol, float scale_h_ref,
     if (!ws_layout(s, L)) return GRPO_ERR_SHAPE;
     *s16 = s;
     s16->dtype = GRPO_BF16;
+    // the pointer and shape checks of the 16-bit path; the workspace is checked against the 8-bit layout
     Inputs in = in8;
     in.shape = s16;
+    in.ws_bytes = ~static_cast<size_t>(0);
     WsLayout L16;
     const int rc = validate(in, &L16);
     if (rc != GRPO_OK) return rc;
-    if (in.ws_bytes < L->total) return GRPO_ERR_WORKSPACE;
+    if (in8.ws_bytes < L->total) return GRPO_ERR_WORKSPACE;
     return GRPO_OK;
 }
 

@@ -181,7 +181,7 @@ def test_validation_codes_of_the_added_entry_points_without_a_device(lib):
     args = lambda shape, ws, dH=P, dW=P, scale=one: (P, P, P, scale, one, one, P, P, P, ctypes.byref(shape), P, ws,  # noqa: E731
                                                      P, dH, dW, None, P, None)
     assert f8(*args(s, need)) == 5                                       # 16-bit shape
-    assert f8(*args(s8, n8 - 1)) == 3                                    # workspace of the 16-bit layout is short
+    assert f8(*args(s8, n8 - 1)) == 3                                    # one byte short of the 8-bit layout
     assert f8(*args(s8, n8, dH=P + 16)) == 1                             # dH only 16-byte aligned
     assert f8(*args(s8, n8, dW=None)) == 1
     assert f8(*args(s8, n8, scale=ctypes.c_float(0.0))) == 2             # a scale must be positive
