@@ -566,7 +566,7 @@ int run_chunked(const Inputs& in, const WsLayout& L, const DeviceInfo& dev, cuda
                     cudaSuccess ||
                 launch(GRPO_PROF_DLOGITS, st, [&] { return launch_transform_f8(cp, dev.sm_count, st); }) !=
                     cudaSuccess ||
-                launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair_fp8(cp, mDS_k, mW_mn, dev.sm_count, st); }) !=
+                launch(GRPO_PROF_DH, st, [&] { return launch_dh_pair_fp8(cp, mDS_k, mW_mn, dev.sm_count, dh_wide, st); }) !=
                     cudaSuccess ||
                 launch(GRPO_PROF_DW, st, [&] { return launch_dw_pair_fp8(cp, mDS_mn, mHc_mn, dev.sm_count, st); }) !=
                     cudaSuccess)

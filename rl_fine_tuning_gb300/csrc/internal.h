@@ -222,7 +222,7 @@ cudaError_t launch_dh_pair(const ChunkParams& p, const CUtensorMap& mDS, const C
 cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const CUtensorMap& mHcmn, int n_sm,
                            bool bf16, cudaStream_t st);
 cudaError_t launch_dh_pair_fp8(const ChunkParams& p, const CUtensorMap& mQa, const CUtensorMap& mWmn, int n_sm,
-                               cudaStream_t st);
+                               bool wide, cudaStream_t st);
 cudaError_t launch_dw_pair_fp8(const ChunkParams& p, const CUtensorMap& mQbmn, const CUtensorMap& mHqmn, int n_sm,
                                cudaStream_t st);
 

@@ -1074,6 +1074,95 @@ struct DhPairF8T5 : DhPairF8T {
     }
 };
 
+// The 8-bit dH in 512-column units (see DhPairWideT): a K-stage of 128 vocabulary
+// rows, two MMAs per K sub-step from one staged code tile, the epilogue of
+// DhPairF8T over both 256-column halves.
+struct DhPairF8WideT : DhPairWideT {
+    static constexpr int kStageElems = 128;
+    __device__ static bool setup(const Params& p, Sched& sc) {
+        if (!DhPairWideT::setup(p, sc)) return false;
+        sc.ks = (p.V + kStageElems - 1) / kStageElems;
+        return true;
+    }
+    __device__ static uint32_t tx_bytes(const Params& p, const Sched&, const Coord& c) {
+        uint32_t b = 2 * 16384;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+                if (c.n0 + h * kBN + r * 128 < p.d) b += 16384;
+        return b;
+    }
+    __device__ static void load(const Params& p, const Sched&, const Coord& c, int k, uint8_t* st, uint32_t bar,
+                                const CUtensorMap* mA, const CUtensorMap*, const CUtensorMap* mB, int rank) {
+        tma_load_2d_pair(mA, bar, st, k * kStageElems, c.m0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int col = c.n0 + h * kBN + rank * 128;
+            if (col < p.d) tma_load_2d_pair(mB, bar, st + 16384 + 16384 * h, col, k * kStageElems);
+        }
+    }
+    template <bool kE5M2>
+    __device__ static void mma_fmt(uint32_t st, uint32_t acc, bool first) {
+        constexpr uint32_t idesc = make_idesc_f8(256, 256, kE5M2, false, true);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t a = desc_kmajor(st + kk * 32);
+            const uint32_t accum = (first && kk == 0) ? 0u : 1u;
+            umma_pair_f8(acc, a, desc_mnmajor_f8(st + 16384 + kk * 4096), idesc, accum);
+            umma_pair_f8(acc + 256, a, desc_mnmajor_f8(st + 32768 + kk * 4096), idesc, accum);
+        }
+    }
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        mma_fmt<false>(st, acc, first);
+    }
+    template <bool>
+    __device__ static void epi_item(const Params& p, const Sched& sc, int unit, int, int rank, uint32_t tacc, Epi&) {
+        const int row = (threadIdx.x & 31) + 32 * ((threadIdx.x >> 5) & 3);
+        const int slot = mtile(sc, unit, rank) * kBM + row;
+        const int n0 = dtile(sc, unit) * 2 * kBN;
+        bool valid = slot < sc.n_c;
+        if (!__any_sync(0xffffffffu, valid)) return;
+        const int t = valid ? p.rows[sc.c0 + slot] : 0;
+        if (valid && !GRPO_DCHECK(t >= 0 && t < p.N, p.status)) valid = false;
+        // a token id outside [0, V) has g = 0 (the merge reported it): no W row is read for it
+        int tok = valid ? p.tokens[t] : 0;
+        const bool tok_ok = tok >= 0 && tok < p.V;
+        if (!tok_ok) tok = 0;
+        const float g = valid && tok_ok ? p.gco[t] : 0.f;
+        const float s_t = valid ? fabsf(g) * expf(p.rmax[t] - p.lse[t]) * (1.f / 448.f) : 0.f;
+        const float f = sc.winv * p.scale_w;
+        uint16_t* out = p.dH + static_cast<int64_t>(t) * p.d;
+        const uint8_t* wrow = p.wq + static_cast<int64_t>(tok) * p.d;
+#pragma unroll 1
+        for (int c = 0; c < 2 * kBN / 32; ++c) {
+            const int col0 = n0 + c * 32;
+            if (col0 >= p.d) break;
+            float v[32];
+            tmem_ld32(tacc + c * 32, v);
+            if (!valid) continue;
+            float wt[32];
+            decode32_f8(wrow + col0, p.e5m2 != 0, wt);
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2)
+                pk[j / 2] = pack2(f * (g * wt[j] - s_t * v[j]), f * (g * wt[j + 1] - s_t * v[j + 1]), true);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                st_global_v8(out + col0 + 16 * h, pk[8 * h], pk[8 * h + 1], pk[8 * h + 2], pk[8 * h + 3],
+                             pk[8 * h + 4], pk[8 * h + 5], pk[8 * h + 6], pk[8 * h + 7]);
+        }
+    }
+};
+
+struct DhPairF8WideT5 : DhPairF8WideT {
+    template <bool>
+    __device__ static void mma(uint32_t st, uint32_t acc, bool first) {
+        mma_fmt<true>(st, acc, first);
+    }
+};
+
 struct DwPairF8T : DwPairT {
     static constexpr int kStageElems = 128;
     __device__ static bool setup(const Params& p, Sched& sc) {
@@ -1432,6 +1521,8 @@ GRPO_PAIR_KERNEL(grpo_dh_pair_wide_kernel, DhPairWideT)
 GRPO_PAIR_KERNEL(grpo_dw_pair_kernel, DwPairT)
 GRPO_PAIR_KERNEL(grpo_dh_pair_e4m3_kernel, DhPairF8T)
 GRPO_PAIR_KERNEL(grpo_dh_pair_e5m2_kernel, DhPairF8T5)
+GRPO_PAIR_KERNEL(grpo_dh_pair_wide_e4m3_kernel, DhPairF8WideT)
+GRPO_PAIR_KERNEL(grpo_dh_pair_wide_e5m2_kernel, DhPairF8WideT5)
 GRPO_PAIR_KERNEL(grpo_dw_pair_e4m3_kernel, DwPairF8T)
 GRPO_PAIR_KERNEL(grpo_dw_pair_e5m2_kernel, DwPairF8T5)
 #undef GRPO_PAIR_KERNEL
@@ -1495,7 +1586,10 @@ cudaError_t launch_dw_pair(const ChunkParams& p, const CUtensorMap& mDSmn, const
 }
 
 cudaError_t launch_dh_pair_fp8(const ChunkParams& p, const CUtensorMap& mQa, const CUtensorMap& mWmn, int n_sm,
-                               cudaStream_t st) {
+                               bool wide, cudaStream_t st) {
+    if (wide)
+        return p.e5m2 ? launch_tc<DhPairF8WideT5, 2>(grpo_dh_pair_wide_e5m2_kernel<true>, p, mQa, mQa, mWmn, n_sm, st)
+                      : launch_tc<DhPairF8WideT, 2>(grpo_dh_pair_wide_e4m3_kernel<true>, p, mQa, mQa, mWmn, n_sm, st);
     return p.e5m2 ? launch_tc<DhPairF8T5, 2>(grpo_dh_pair_e5m2_kernel<true>, p, mQa, mQa, mWmn, n_sm, st)
                   : launch_tc<DhPairF8T, 2>(grpo_dh_pair_e4m3_kernel<true>, p, mQa, mQa, mWmn, n_sm, st);
 }

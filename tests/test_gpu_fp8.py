@@ -234,3 +234,13 @@ def test_fp8_backward_objective_variants_and_sequence_mean(objective):
     res, exp = run_fp8_bwd(synth.generate_fp8(cfg, seed=48, fmt="e4m3"), chunk_rows=256, objective=objective,
                            loss_mode=1)
     assert_fp8_grad_parity(res, exp)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+def test_fp8_backward_wide_dh_units(fmt):
+    # the default 76-tile chunks with d = 768: 38 tile pairs x 2 wide d tiles of 512 columns divide over
+    # the 76 SM pairs, so the 8-bit dH runs in 512-column units, the second one half past d
+    cfg = synth.make_config("tiny", G=4, L=4096, d=768, V=1000, len_lo=1500, len_hi=4096)
+    res, exp = run_fp8_bwd(synth.generate_fp8(cfg, seed=31, fmt=fmt))
+    assert exp["n_valid"] > 76 * 128             # two chunks
+    assert_fp8_grad_parity(res, exp)
