@@ -87,3 +87,22 @@ def test_workload_description():
     d = bench.cfg_dict(cfg, {"n_valid": 1})
     assert d["workload"] == "llama-3.1-8b-20k" and d["N"] == 160000 and d["V"] == 128256
     assert d["parallelism"] == "replicas" and d["n_valid"] == 1
+
+
+def test_traffic_lookup_takes_the_committed_median_only_for_the_current_source(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    entry = {"kernel": "grpo_fwd_pair_kernel", "dram_bytes_per_launch_full_workload": 7,
+             "captures": [6, 7, 9], "spread": [6, 9]}
+    doc = {"kernel_source_hash": bench.kernel_source_hash(), "chunk_rows": 4864, "kernels": {"fwd": entry}}
+    (prof / "traffic.json").write_text(json.dumps(doc))
+    src = os.path.join(ROOT, "rl_fine_tuning_gb300")
+    os.symlink(src, tmp_path / "rl_fine_tuning_gb300")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.ncu_traffic("fwd", 4864) == 7
+    assert bench.ncu_traffic("fwd", 4864, "spread") == [6, 9]
+    assert bench.ncu_traffic("fwd", 9728) is None          # another chunk height
+    assert bench.ncu_traffic("dh", 4864) is None           # not captured
+    doc["kernel_source_hash"] = "0" * 16                    # counters of another kernel source
+    (prof / "traffic.json").write_text(json.dumps(doc))
+    assert bench.ncu_traffic("fwd", 4864) is None
