@@ -328,7 +328,8 @@ def run_ours(args, ranks):
     N, d, V = cfg.N, cfg.d, cfg.V
     adv = torch.empty(cfg.n_seq, dtype=torch.float32, device="cuda")
     mask = torch.empty(N, dtype=torch.uint8, device="cuda")
-    split = ranks.dev_group is not None
+    # (with one rank the split is the whole batch, still through the shard entry points)
+    split = args.split
 
     def outputs():
         return {"dH": torch.empty((N, d), dtype=tdt, device="cuda"),
@@ -622,6 +623,7 @@ def run_ours(args, ranks):
         "loss": float(out["loss"].item()),
         "parallelism": ("data-parallel shards: one prompt group per rank, batch counts, loss shares and dW summed "
                         "over the ranks every step" if split else "replicas"),
+        "split": bool(split),
     }
     if ranks.rank == 0:
         print(json.dumps(line), flush=True)
