@@ -1,6 +1,13 @@
 """Writes the full-mask expected values of a model-head workload, from the fp64 oracle only.
 
     python tests/golden/make_fullmask_golden.py WORKLOAD [WORKLOAD ...]
+    python tests/golden/make_fullmask_golden.py --completion I WORKLOAD
+
+The second form masks the workload to the rows of completion I alone (all its
+generated rows, the other completions masked out) and writes
+``tests/golden/completion<I>_<WORKLOAD>.npz``: the same values for a batch
+whose masked-in rows fill several backward chunks of the full-size shape, at
+an oracle cost of one completion.
 
 For each workload (a name in ``synth.CONFIGS``) it generates the seeded
 inputs (seed 0), builds the completion mask from the generated lengths and
@@ -62,12 +69,23 @@ def pick_vrows(cfg, tokens_valid: np.ndarray) -> np.ndarray:
     return np.array(sorted(pick), np.int32)
 
 
-def make(name: str) -> str:
+def completion_mask(cfg, lengths, i: int) -> np.ndarray:
+    """The completion mask of the workload with every completion but i masked out."""
+    full = oracle.build_mask(lengths, cfg.L)
+    mask = np.zeros_like(full)
+    mask[i * cfg.L:(i + 1) * cfg.L] = full[i * cfg.L:(i + 1) * cfg.L]
+    return mask
+
+
+def make(name: str, completion=None) -> str:
     cfg = synth.CONFIGS[name]
     t0 = time.time()
     wl = synth.generate(cfg, seed=SEED)
     adv = oracle.group_advantages(wl.rewards, cfg.n_groups, cfg.G, cfg.eps, True)
-    mask = oracle.build_mask(wl.lengths, cfg.L)
+    if completion is None:
+        mask = oracle.build_mask(wl.lengths, cfg.L)
+    else:
+        mask = completion_mask(cfg, wl.lengths, completion)
     rows = oracle.valid_rows(mask)
     terms = oracle.row_terms(wl.h_pol, wl.h_ref, wl.W, cfg.dtype, wl.tokens, adv, cfg.L, rows, cfg.beta)
     loss = oracle.reduce_loss(terms["ell"], rows, cfg.L)
@@ -75,22 +93,29 @@ def make(name: str) -> str:
     vrows = pick_vrows(cfg, wl.tokens[rows])
     _, dW = oracle.grad(wl.h_pol, wl.W, cfg.dtype, wl.tokens, rows, terms["lse_pol"], terms["g"], w,
                         want_dH=False, vrows=vrows, want_dW=True)
-    path = out_path(name)
+    path = out_path(name) if completion is None else os.path.join(HERE, f"completion{completion}_{name}.npz")
+    cmd = f"python tests/golden/make_fullmask_golden.py {name}" if completion is None else \
+        f"python tests/golden/make_fullmask_golden.py --completion {completion} {name}"
     np.savez(path, workload=np.array(name), seed=np.array(SEED), fingerprint=np.array(fingerprint(wl)),
+             completion=np.array(-1 if completion is None else completion),
              n_valid=np.array(rows.size, np.int64), loss=np.array(loss, np.float64),
              pen_mean=np.array(float(np.mean(terms["pen"])), np.float64), rows=rows.astype(np.int32),
              lse_pol=terms["lse_pol"].astype(np.float32), lse_ref=terms["lse_ref"].astype(np.float32),
              q=terms["q"].astype(np.float32), p=terms["p"].astype(np.float32),
              pen=terms["pen"].astype(np.float32), vrows=vrows, dW_rows=dW.astype(np.float32),
-             command=np.array(f"python tests/golden/make_fullmask_golden.py {name}"))
+             command=np.array(cmd))
     print(f"{name}: N_v {rows.size}, loss {loss:.9f}, {time.time() - t0:.0f} s -> {path}", flush=True)
     return path
 
 
 if __name__ == "__main__":
-    if len(sys.argv) < 2:
+    args = sys.argv[1:]
+    if not args:
         raise SystemExit(__doc__)
     oracle.build()
     synth.build()
-    for n in sys.argv[1:]:
-        make(n)
+    if args[0] == "--completion":
+        make(args[2], completion=int(args[1]))
+    else:
+        for n in args:
+            make(n)

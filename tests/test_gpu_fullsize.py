@@ -158,6 +158,55 @@ def load_golden(cfg):
     return g
 
 
+def test_single_completion_against_golden(big):
+    """The full-size shape in the benchmark's launch configuration, masked to one completion whose rows fill
+    several backward chunks (default height), against the oracle's values for every row, where
+    tests/golden holds them (completion<I>_<workload>.npz, written by make_fullmask_golden.py --completion I)."""
+    import glob
+    cfg = big.cfg
+    files = sorted(glob.glob(os.path.join(GOLDEN, f"completion*_{cfg.name}.npz")))
+    if not files:
+        pytest.skip(f"no single-completion golden values for {cfg.name}")
+    import sys
+    sys.path.insert(0, GOLDEN)
+    from make_fullmask_golden import completion_mask, fingerprint
+    g = np.load(files[0])
+    assert str(g["workload"]) == cfg.name and int(g["seed"]) == 0
+    assert fingerprint(big) == str(g["fingerprint"]), "regenerated inputs differ from the golden file's"
+    mask = completion_mask(cfg, big.lengths, int(g["completion"]))
+    rows = oracle.valid_rows(mask)
+    assert np.array_equal(rows, g["rows"]) and rows.size == int(g["n_valid"])
+    dw = DeviceWorkload(big, mask=mask)
+    assert rows.size > 2 * rg_chunk_rows(dw)                 # at least two full chunks and a partial one
+    scale = run_scaled(dw, cfg)
+    sample = rows[np.random.default_rng(29).choice(rows.size, size=8, replace=False)]
+    res = light_results(dw, np.sort(sample), scale)
+    vr = torch.from_numpy(g["vrows"].astype(np.int64)).cuda()
+    dW_rows = dw.dW.index_select(0, vr).cpu().numpy().astype(np.float64) / scale
+    del dw
+    torch.cuda.empty_cache()
+    assert res["status"] == 0
+    g_loss = float(g["loss"])
+    assert abs(res["loss"] - g_loss) <= 1e-3 * abs(g_loss), (res["loss"], g_loss)
+    rs = res["row_stats"][rows]
+    for col, key in ((0, "lse_pol"), (1, "lse_ref"), (2, "q"), (3, "p")):
+        ref = g[key].astype(np.float64)
+        assert np.all(np.abs(rs[:, col] - ref) <= 1e-3 * np.maximum(1.0, np.abs(ref))), key
+    pen = g["pen"].astype(np.float64)
+    assert np.all(np.abs(rs[:, 4] - pen) <= 1e-5 + 1e-2 * np.abs(pen))
+    ref_dW = g["dW_rows"].astype(np.float64)
+    assert np.abs(dW_rows - ref_dW).max() <= 2e-2 * np.abs(ref_dW).max()
+    exp = oracle.expected(big, mask=mask, eval_rows=np.sort(sample), want_dW=False)
+    assert np.abs(res["dH_rows"] / scale - exp["dH"]).max() <= 2e-2 * np.abs(exp["dH"]).max()
+    assert res["dH_masked_zero"] and res["dH_finite"]
+    assert_pairing(res["pairing"])
+
+
+def rg_chunk_rows(dw):
+    import rl_fine_tuning_gb300 as rg
+    return rg.grpo_chunk_rows(dw.shape)
+
+
 def test_full_mask_sampled_rows(big):
     cfg = big.cfg
     mask = oracle.build_mask(big.lengths, cfg.L)
