@@ -14,8 +14,15 @@
 //   grpo_fwd_pair_e4m3_kernel, grpo_fwd_pair_e5m2_kernel  the same forward
 //         on 8-bit inputs (kind::f8f6f4), scaled by the per-tensor scales.
 //   grpo_dh_pair_kernel   dH[rows] = (1/N_valid) * dlogits . W        (K = vocabulary)
+//   grpo_dh_pair_wide_kernel  the same in 512-column units: one staged
+//         dlogits tile feeds two 256-wide d tiles, the whole tensor memory
+//         one accumulator (where those units divide evenly over the pairs)
 //   grpo_dw_pair_kernel   dW      += (1/N_valid) * dlogits^T . H_pol  (K = chunk rows; H_pol from
 //         the transposed compact rows, so its operand is K-major)
+//   grpo_dh_pair_{,wide_}{e4m3,e5m2}_kernel, grpo_dw_pair_{e4m3,e5m2}_kernel
+//         the backward on 8-bit codes (kind::f8f6f4, MN-major 8-bit operands):
+//         the dlogits' softmax part as codes scaled per row (dH) or per 32
+//         vocabulary rows (dW), the one-hot part added exactly in the epilogue
 // Single-SM kernel (tcgen05.mma.cta_group::1, M = 128):
 //   grpo_fwd_lse_kernel   the forward over row tiles of h_pol / h_ref (the
 //         workspace-free entry point), policy and reference MMAs sharing B.
@@ -26,9 +33,10 @@
 //   warps 2..5  epilogue; warp w reads TMEM lanes 32*(w%4) .. 32*(w%4)+31,
 //               i.e. one accumulator row per thread.
 // Stages: smem ring of kStages K-slices (64 elements = one 128-byte swizzle
-// span), full/empty mbarriers; accumulators: double-buffered in TMEM (except
-// the single-SM forward, whose two accumulators are the policy and reference
-// tiles) with acc_full/acc_empty mbarriers, so the epilogue of one tile
+// span; 128 for 8-bit operands), full/empty mbarriers; accumulators:
+// double-buffered in TMEM (except the single-SM forward, whose two
+// accumulators are the policy and reference tiles, and the 512-column dH
+// units) with acc_full/acc_empty mbarriers, so the epilogue of one tile
 // overlaps the MMAs of the next.
 #include <cmath>
 #include <cuda_bf16.h>
