@@ -792,6 +792,19 @@ __device__ __forceinline__ uint32_t f8x2(float x0, float x1, bool e5m2) {
 //   qb = P * 448 / gmax[grp]                                                 (per group)
 // Columns past V and rows past the chunk's last (to the next multiple of 128)
 // get code 0.
+// 32-byte global load / store (one whole L2 sector per thread); 32-byte aligned addresses
+__device__ __forceinline__ void ld_sector(const void* a, uint32_t (&v)[8]) {
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "l"(a));
+}
+
+__device__ __forceinline__ void st_sector(void* a, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(a), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 __global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkParams p) {
     if (p.chunk >= p.counts[C_NCHUNKS]) return;
     const int rc = p.counts[C_CHUNK_ROWS];
@@ -799,17 +812,19 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkP
     const int n_c = min(rc, p.counts[C_NVALID] - c0);
     const int n_fill = min(p.R, (n_c + kBM - 1) / kBM * kBM);
     // one 32-column group per thread and step (its two scale factors are the group's):
-    // 64 bytes of exponentials in, 32 bytes of each code out
+    // 64 bytes of exponentials in, 32 bytes of each code out, all as whole 32-byte sectors
+    // (the buffers are 256-byte aligned and V_pad is a multiple of 64)
     const int ngrp = p.V_pad / 32;
     const bool e5 = p.e5m2 != 0;
     for (int slot = blockIdx.x; slot < n_fill; slot += gridDim.x) {
-        const uint4* erow = reinterpret_cast<const uint4*>(p.dS + static_cast<int64_t>(slot) * p.V_pad);
-        uint4* arow = reinterpret_cast<uint4*>(p.qa + static_cast<int64_t>(slot) * p.V_pad);
-        uint4* brow = reinterpret_cast<uint4*>(p.qb + static_cast<int64_t>(slot) * p.V_pad);
+        const uint16_t* erow = p.dS + static_cast<int64_t>(slot) * p.V_pad;
+        uint8_t* arow = p.qa + static_cast<int64_t>(slot) * p.V_pad;
+        uint8_t* brow = p.qb + static_cast<int64_t>(slot) * p.V_pad;
         if (slot >= n_c) {
-            for (int i = threadIdx.x; i < 2 * ngrp; i += kTransformThreads) {
-                arow[i] = make_uint4(0, 0, 0, 0);
-                brow[i] = make_uint4(0, 0, 0, 0);
+            const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+            for (int grp = threadIdx.x; grp < ngrp; grp += kTransformThreads) {
+                st_sector(arow + 32 * grp, z);
+                st_sector(brow + 32 * grp, z);
             }
             continue;
         }
@@ -831,12 +846,13 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkP
                 const float ca = sa * expf(m - zmax);
                 const float gm = p.gmax[grp];
                 const float cb = gm > 0.f ? g * expf(m - lse) * (448.f / gm) : 0.f;
-                uint4 u[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) u[j] = erow[4 * grp + j];
+                uint32_t u[2][8];
+                ld_sector(erow + 32 * grp, u[0]);
+                ld_sector(erow + 32 * grp + 16, u[1]);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const uint32_t w[4] = {u[j].x, u[j].y, u[j].z, u[j].w};
+                    const uint32_t w[4] = {u[j >> 1][4 * (j & 1)], u[j >> 1][4 * (j & 1) + 1],
+                                           u[j >> 1][4 * (j & 1) + 2], u[j >> 1][4 * (j & 1) + 3]};
                     uint32_t pa[4], pb[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -852,10 +868,8 @@ __global__ void __launch_bounds__(kTransformThreads) k_transform_f8(const ChunkP
                     ob[2 * j + 1] = pb[2] | (pb[3] << 16);
                 }
             }
-            arow[2 * grp] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-            arow[2 * grp + 1] = make_uint4(oa[4], oa[5], oa[6], oa[7]);
-            brow[2 * grp] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-            brow[2 * grp + 1] = make_uint4(ob[4], ob[5], ob[6], ob[7]);
+            st_sector(arow + 32 * grp, oa);
+            st_sector(brow + 32 * grp, ob);
         }
     }
 }
