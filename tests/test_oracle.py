@@ -279,6 +279,46 @@ def test_row_terms_against_numpy_scipy():
     assert np.allclose(t["g"], -A + 0.04 * (1 - np.exp(x)), atol=1e-12)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_16bit_row_loops_read_storage_as_numpy_and_torch_widen_it(dtype):
+    # The row loops read 16-bit storage (fp16 through its table of all 65536 patterns).  Given the bit
+    # patterns, every row term and gradient must equal, bit for bit, the fp64 path on the values that numpy
+    # (fp16) or torch (bf16) widens the same patterns to: same values, same ascending-index sums.
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    G, L, d, V = 3, 4, 40, 70
+    N = G * L
+    h = rng.normal(size=(N, d)) * 3.0
+    x = {"h_pol": h, "h_ref": h + 0.1 * rng.normal(size=(N, d)), "W": rng.normal(size=(V, d)) * 0.3}
+    if dtype == "fp16":
+        for k in x:                                      # fp16 subnormals and a large normal value
+            x[k][0, :3] = [1e-6, -3e-8, 900.0]
+    bits = {}
+    for name, v in x.items():
+        if dtype == "fp16":
+            bits[name] = v.astype(np.float16).view(np.uint16)
+        else:
+            bits[name] = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy() \
+                .view(np.uint16)
+    if dtype == "fp16":
+        val = {k: b.view(np.float16).astype(np.float64) for k, b in bits.items()}
+    else:
+        val = {k: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+               for k, b in bits.items()}
+    tok = rng.integers(0, V, N).astype(np.int32)
+    adv = oracle.group_advantages(rng.normal(size=G).astype(np.float32), 1, G)
+    rows = np.arange(N, dtype=np.int32)
+    t16 = oracle.row_terms(bits["h_pol"], bits["h_ref"], bits["W"], dtype, tok, adv, L, rows)
+    t64 = oracle.row_terms(val["h_pol"], val["h_ref"], val["W"], "f64", tok, adv, L, rows)
+    for k in t16:
+        assert np.all(np.isfinite(t16[k])) and np.array_equal(t16[k], t64[k]), k
+    w = oracle.row_weights(rows, L)
+    g16 = oracle.grad(bits["h_pol"], bits["W"], dtype, tok, rows, t16["lse_pol"], t16["g"], w)
+    g64 = oracle.grad(val["h_pol"], val["W"], "f64", tok, rows, t64["lse_pol"], t64["g"], w)
+    for a16, a64 in zip(g16, g64):
+        assert np.all(np.isfinite(a16)) and np.array_equal(a16, a64)
+
+
 def test_kl_small_argument_taylor():
     # p - q tiny: KL ~ x^2/2 + x^3/6 with no cancellation loss
     rng = np.random.default_rng(4)
