@@ -112,17 +112,21 @@ double oracle_e5m2_to_f64(uint8_t b) {
     return sign ? -v : v;
 }
 
-/* The fp16 value of every bit pattern, filled by oracle_f16_to_f64 when the
- * library loads: the same values, without a libm call per element in the
+/* The value of every bf16 and fp16 bit pattern, filled by the decoders above
+ * when the library loads: the same values, without a call per element in the
  * row loops below. */
+static double bf16_value[65536];
 static double f16_value[65536];
 
-__attribute__((constructor)) static void fill_f16_values(void) {
-    for (uint32_t b = 0; b < 65536u; ++b) f16_value[b] = oracle_f16_to_f64((uint16_t)b);
+__attribute__((constructor)) static void fill_16bit_values(void) {
+    for (uint32_t b = 0; b < 65536u; ++b) {
+        bf16_value[b] = oracle_bf16_to_f64((uint16_t)b);
+        f16_value[b] = oracle_f16_to_f64((uint16_t)b);
+    }
 }
 
 static inline double ld(const void* p, int type, size_t i) {
-    if (type == OR_BF16) return oracle_bf16_to_f64(((const uint16_t*)p)[i]);
+    if (type == OR_BF16) return bf16_value[((const uint16_t*)p)[i]];
     if (type == OR_F16) return f16_value[((const uint16_t*)p)[i]];
     return ((const double*)p)[i];
 }
@@ -194,7 +198,7 @@ static inline double dot_w(const double* h, const void* W, int type, int v, int 
     double acc = 0.0;
     if (type == OR_BF16) {
         const uint16_t* w = (const uint16_t*)W + (size_t)v * d;
-        for (int k = 0; k < d; ++k) acc = acc + h[k] * oracle_bf16_to_f64(w[k]);
+        for (int k = 0; k < d; ++k) acc = acc + h[k] * bf16_value[w[k]];
     } else if (type == OR_F16) {
         const uint16_t* w = (const uint16_t*)W + (size_t)v * d;
         for (int k = 0; k < d; ++k) acc = acc + h[k] * f16_value[w[k]];
