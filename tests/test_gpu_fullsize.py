@@ -158,6 +158,14 @@ def load_golden(cfg):
     return g
 
 
+def _completion_golden_workloads():
+    """Workloads for which tests/golden holds single-completion values (completion<I>_<workload>.npz)."""
+    import glob
+    names = {os.path.basename(f)[:-4].split("_", 1)[1] for f in glob.glob(os.path.join(GOLDEN, "completion*_*.npz"))}
+    return [n for n in BIG if n in names]
+
+
+@pytest.mark.parametrize("big", _completion_golden_workloads(), indirect=True)
 def test_single_completion_against_golden(big):
     """The full-size shape in the benchmark's launch configuration, masked to one completion whose rows fill
     several backward chunks (default height), against the oracle's values for every row, where
@@ -165,8 +173,6 @@ def test_single_completion_against_golden(big):
     import glob
     cfg = big.cfg
     files = sorted(glob.glob(os.path.join(GOLDEN, f"completion*_{cfg.name}.npz")))
-    if not files:
-        pytest.skip(f"no single-completion golden values for {cfg.name}")
     import sys
     sys.path.insert(0, GOLDEN)
     from make_fullmask_golden import completion_mask, fingerprint
